@@ -1,0 +1,394 @@
+"""Benchmark of the BA-Att hot path on GB300: select + block-sparse attention.
+
+One step = ba_select (norm sort, block statistics, compensated scores,
+top-kappa) followed by ba_sparse_attn over one batch of the headline workload
+(b1, 32 heads, L=65536, d=128, B=128, 50% sparsity, sort Q and K, beta 1),
+synthetic seeded inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload ultra64k] [--no-cpu-baseline]
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own batch
+(heads are independent: weak scaling, no collective on the data path); the
+ranks meet at a barrier around the timed region and rank 0 reports the
+maximum time.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ms & dense-equiv TFLOPS, select+sparse attn, L=64k 50% sparsity; select GB/s"
+UNIT = "TFLOPS (dense-equivalent 4*b*h*L^2*d per step / step time)"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p["bf16_tflops_sustained"]), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def dense_flops(w):
+    return 4.0 * w.batch * w.heads * w.seqlen * w.seqlen * w.head_dim
+
+
+def select_bytes(w, sort_q=True, sort_k=True):
+    """Algorithmic bytes of the selection stage: Q and K are streamed once for
+    the norms of each sorted tensor and once for the block statistics; small
+    outputs (pi, index list, mask) are added."""
+    t = w.batch * w.heads * w.seqlen * w.head_dim * 2
+    reads = (2 if sort_q else 1) * t + (2 if sort_k else 1) * t
+    N = w.nblocks
+    kappa = w.kappa()
+    writes = (2 * w.batch * w.heads * w.seqlen * 4
+              + w.batch * w.heads * N * (kappa * 4 + ((N + 31) // 32) * 4))
+    return reads + writes
+
+
+def launches_per_step(w):
+    """Kernels the library launches per step (select + sparse attention) for
+    sort mode QK: per sorted tensor 1 norm pass, 1 chunk sort and
+    ceil(log2(L / 4096)) merge passes; 2 statistics, 1 score and 1 top-kappa
+    kernel; then 2 row gathers (Q, and K with V) and the attention kernel."""
+    passes = 0
+    width = 4096
+    while width < w.seqlen:
+        width *= 2
+        passes += 1
+    select = 2 * (2 + passes) + 2 + 1 + 1
+    attn = 2 + 1
+    return select + attn
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"], samples=0)
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None, sm_max_mhz=max(mx) if mx else None,
+                    reasons=sorted(reasons), samples=len(sm))
+
+
+def cpu_oracle_sample(w, q, k, v, budget_s=12.0, seed=0):
+    """Times the fp64 oracle on one head: its whole selection plus as many
+    sampled query blocks of attention as fit in ``budget_s``; extrapolates
+    to the head's full work and returns dense-equivalent TFLOPS."""
+    import numpy as np
+
+    import oracle.ba_oracle as O
+    kappa = w.kappa()
+    Q = q[0, 0].double().numpy()
+    K = k[0, 0].double().numpy()
+    V = v[0, 0].double().numpy()
+    t0 = time.perf_counter()
+    sel = O.select_one(Q, K, w.block, kappa, 1.0, O.SORT_QK)
+    t_sel = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.nblocks)
+    done = 0
+    t1 = time.perf_counter()
+    while done < len(order) and (done < 4 or time.perf_counter() - t1 < budget_s):
+        O.sparse_attention_one(Q, K, V, sel["perm_q"], sel["perm_k"], sel["idx"], w.block,
+                               query_blocks=[int(order[done])])
+        done += 1
+    t_att = time.perf_counter() - t1
+    per_head = t_sel + t_att / done * w.nblocks
+    head_flops = 4.0 * w.seqlen * w.seqlen * w.head_dim
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dict(value=head_flops / per_head / 1e12, unit=UNIT, cores=cores, kind="oracle",
+                sample=(f"1 of {w.heads} heads: full selection ({t_sel:.2f} s) + {done} of "
+                        f"{w.nblocks} query blocks of attention ({t_att:.2f} s), extrapolated "
+                        f"linearly to the head ({per_head:.1f} s); fp64 numpy"),
+                seconds=t_sel + t_att)
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores of rank 0."""
+    import workloads
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = workloads.get(args.workload)
+    q, k, v, _ = workloads.make_inputs(w)
+    values = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(w, q, k, v, budget_s=max(2.0, 60.0 / max(1, args.steps + args.warmup)), seed=i)
+        if i >= args.warmup:
+            values.append(r)
+    val = statistics.median(x["value"] for x in values)
+    head_ms = dense_flops(w) / w.heads / (val * 1e12) * 1e3
+    out = dict(impl="reference", metric=METRIC, value=val, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
+               warmup=args.warmup, ms_per_step=head_ms * w.heads, higher_is_better=True,
+               scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+               config=workload_config(w),
+               cpu_baseline=dict(value=val, unit=UNIT, cores=values[-1]["cores"], kind="oracle",
+                                 sample=values[-1]["sample"]),
+               e2e=dict(value=val, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+               gpu_launches=0)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return dict(workload=(f"{w.name}: b{w.batch} h{w.heads} L{w.seqlen} d{w.head_dim} B{w.block} "
+                          f"kappa{w.kappa()} ({int(w.sparsities[0] * 100)}% sparsity), sort QK, beta 1"),
+                global_batch=w.batch, seq_len=w.seqlen, heads=w.heads, head_dim=w.head_dim,
+                block=w.block, kappa=w.kappa(),
+                l2=f"inputs {3 * w.batch * w.heads * w.seqlen * w.head_dim * 2 / 2**30:.2f} GiB > L2, no flush",
+                parallelism="independent heads per GPU (no collective)")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ultra64k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dense-steps", type=int, default=3)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_bidirectional_gb300 as bsb
+    import workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    w = workloads.get(args.workload)
+    kappa = w.kappa()
+    q, k, v, _ = workloads.make_inputs(w, seed=w.seed + rank)
+    b, h, L, d, B = w.batch, w.heads, w.seqlen, w.head_dim, w.block
+    N = w.nblocks
+    bsb.load()
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    # outputs and workspaces allocated once, outside the timed region
+    i32 = dict(dtype=torch.int32, device=dev)
+    perm_q = torch.empty((b, h, L), **i32)
+    perm_k = torch.empty((b, h, L), **i32)
+    idx = torch.empty((b, h, N, kappa), **i32)
+    mask = torch.empty((b, h, N, (N + 31) // 32), **i32)
+    ws_sel = torch.empty(bsb.select_workspace_size(b, h, L, d, B, kappa, 3, 0), dtype=torch.uint8, device=dev)
+    ws_att = torch.empty(bsb.sparse_attn_workspace_size(b, h, L, d, B, kappa), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((b, h, L), dtype=torch.float32, device=dev)
+
+    def step(qx, kx, vx):
+        bsb.ba_select_into(qx, kx, B, kappa, 1.0, 3, 0, perm_q, perm_k, idx, mask, None, ws_sel)
+        bsb.ba_sparse_attn_into(qx, kx, vx, B, perm_q, perm_k, idx, 0.0, o, lse, ws_att)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step(qd, kd, vd)
+    torch.cuda.synchronize(dev)
+    st, word = bsb.last_device_error(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} after warm-up")
+
+    # algorithmic attention FLOPs from the emitted mask (4 d per selected
+    # query-key pair; the ragged last block counts its real tokens)
+    sizes = np.full(N, B, dtype=np.float64)
+    sizes[-1] = L - (N - 1) * B
+    idx_np = idx.cpu().numpy()
+    pair_tokens = sizes[idx_np].sum(axis=-1)            # [b,h,N]: keys per query block
+    attn_flops = float(4.0 * d * (pair_tokens * sizes[None, None, :]).sum())
+
+    # ---- timed region: K steps, events per stage ----------------------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        bsb.ba_select_into(qd, kd, B, kappa, 1.0, 3, 0, perm_q, perm_k, idx, mask, None, ws_sel)
+        ev[i][1].record(stream)
+        bsb.ba_sparse_attn_into(qd, kd, vd, B, perm_q, perm_k, idx, 0.0, o, lse, ws_att)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end))
+    sel_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    att_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    st, word = bsb.last_device_error(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} in the timed region")
+    ms_step = total_ms / args.steps
+
+    # ---- the library's dense kernel at the same shape -----------------------
+    od = torch.empty_like(qd)
+    lsed = torch.empty_like(lse)
+    bsb.ba_attn_dense_into(qd, kd, vd, 0.0, od, lsed)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.dense_steps):
+        bsb.ba_attn_dense_into(qd, kd, vd, 0.0, od, lsed)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = e0.elapsed_time(e1) / args.dense_steps
+    del od, lsed
+
+    # ---- end to end through the public API from pinned host memory ----------
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qx, kx, vx = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    e2e_steps = max(3, min(args.steps, 5))
+    for _ in range(2):
+        qx.copy_(qh, non_blocking=True); kx.copy_(kh, non_blocking=True); vx.copy_(vh, non_blocking=True)
+        step(qx, kx, vx)
+        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qx.copy_(qh, non_blocking=True); kx.copy_(kh, non_blocking=True); vx.copy_(vh, non_blocking=True)
+        step(qx, kx, vx)
+        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+
+    pk = peaks()
+    flops_step = dense_flops(w)
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    att_tflops = attn_flops / (att_ms * 1e-3) / 1e12
+    sel_b = select_bytes(w)
+    sel_gbs = sel_b / (sel_ms * 1e-3) / 1e9
+    out = dict(
+        metric=METRIC, value=round(value, 3), unit=UNIT, n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=round(ms_step, 4), higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="bf16", data="synthetic", config=workload_config(w),
+        roofline=dict(bound="tensor", achieved=round(att_tflops, 2), peak=pk["bf16"], unit="TFLOP/s",
+                      frac=round(att_tflops / pk["bf16"], 4), traffic=None,
+                      kernel="ba_sparse_attn (row gathers + tcgen05 attention kernel)",
+                      peak_kind=f"bf16 dense burst, {pk['source']}",
+                      algorithmic_flops_per_launch=attn_flops),
+        e2e=dict(value=round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 3), unit=UNIT,
+                 ms_per_step=round(e2e_ms, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+        gpu_launches=launches_per_step(w) * args.steps,
+        clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
+                    samples=clk["samples"]),
+        detail=dict(
+            select_ms=round(sel_ms, 4), attn_ms=round(att_ms, 4),
+            select_gbs=round(sel_gbs, 1), select_bytes=sel_b,
+            select_frac_hbm_measured=round(sel_gbs / pk["hbm"], 4),
+            select_frac_hbm_nominal_8tbs=round(sel_gbs / 8000.0, 4),
+            attn_actual_tflops=round(att_tflops, 2),
+            attn_frac_tensor_burst=round(att_tflops / pk["bf16"], 4),
+            attn_frac_tensor_sustained=round(att_tflops / pk["bf16_sus"], 4),
+            dense_ms=round(dense_ms, 3),
+            dense_tflops=round(flops_step / (dense_ms * 1e-3) / 1e12, 2),
+            dense_frac_tensor_burst=round(flops_step / (dense_ms * 1e-3) / 1e12 / pk["bf16"], 4),
+            speedup_vs_dense=round(dense_ms / ms_step, 3),
+            density=round(attn_flops / flops_step, 4)),
+    )
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = {kk: vv for kk, vv in cpu_oracle_sample(w, q, k, v).items() if kk != "seconds"}
+    elif rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = None
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

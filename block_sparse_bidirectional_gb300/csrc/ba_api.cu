@@ -1,0 +1,223 @@
+// C ABI of the BA-Att library: argument checks, workspace sizing, dispatch.
+// The operations are specified in include/ba.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/ba.h"
+#include "ba_common.cuh"
+#include "ba_internal.h"
+
+namespace ba {
+
+namespace {
+
+constexpr int kMaxBlocksPerSeq = 4096;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every call.  Returns BA_OK or an error status.
+int check_shape(int batch, int heads, int seqlen, int head_dim, int block) {
+  if (batch < 1 || heads < 1 || seqlen < 1) return BA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return BA_ERR_UNSUPPORTED;
+  if (block != 64 && block != 128) return BA_ERR_UNSUPPORTED;
+  const int64_t rows = static_cast<int64_t>(batch) * heads * seqlen;
+  if (rows * head_dim >= (static_cast<int64_t>(1) << 40)) return BA_ERR_UNSUPPORTED;
+  if (rows >= (static_cast<int64_t>(1) << 31)) return BA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(batch) * heads > 65535) return BA_ERR_UNSUPPORTED;
+  const int n = (seqlen + block - 1) / block;
+  if (n > kMaxBlocksPerSeq) return BA_ERR_UNSUPPORTED;
+  return BA_OK;
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? BA_OK : BA_ERR_CUDA; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn resolve_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t encode_tensor_map_3d(void *map_out, const void *base, uint64_t inner, uint64_t rows,
+                                 uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = resolve_encode();
+  if (fn == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {inner, rows, outer};
+  const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(static_cast<CUtensorMap *>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace ba
+
+using namespace ba;
+
+extern "C" {
+
+const char *ba_status_string(int status) {
+  switch (status) {
+    case BA_OK: return "BA_OK";
+    case BA_ERR_INVALID_ARG: return "BA_ERR_INVALID_ARG: invalid argument";
+    case BA_ERR_UNSUPPORTED: return "BA_ERR_UNSUPPORTED: shape or option not supported";
+    case BA_ERR_WORKSPACE: return "BA_ERR_WORKSPACE: workspace too small or misaligned";
+    case BA_ERR_CUDA: return "BA_ERR_CUDA: CUDA runtime or launch error";
+    case BA_ERR_DEVICE_TIMEOUT: return "BA_ERR_DEVICE_TIMEOUT: a kernel gave up on a bounded wait";
+    default: return "BA_ERR_UNKNOWN";
+  }
+}
+
+const char *ba_version(void) { return "ba-gb300 0.1 sm_103a"; }
+
+size_t ba_select_workspace_size(int batch, int heads, int seqlen, int head_dim, int block,
+                                int kappa, int sort_mode, int sort_window) {
+  (void)kappa;
+  (void)sort_window;
+  if (check_shape(batch, heads, seqlen, head_dim, block) != BA_OK) return 0;
+  if (sort_mode < 0 || sort_mode > 3) return 0;
+  return select_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim, block,
+                                sort_mode);
+}
+
+int ba_select(const void *q, const void *k, int batch, int heads, int seqlen, int head_dim,
+              int block, int kappa, float beta, int sort_mode, int sort_window, int32_t *perm_q,
+              int32_t *perm_k, int32_t *block_idx, uint32_t *block_mask, float *block_scores,
+              void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+  int st = check_shape(batch, heads, seqlen, head_dim, block);
+  if (st != BA_OK) return st;
+  const int n = (seqlen + block - 1) / block;
+  if (kappa < 1 || kappa > n) return BA_ERR_INVALID_ARG;
+  if (!isfinite(beta)) return BA_ERR_INVALID_ARG;
+  if (sort_mode < 0 || sort_mode > 3) return BA_ERR_INVALID_ARG;
+  if (sort_window < 0 || (sort_window > 0 && sort_window % block != 0)) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !perm_q || !perm_k || !block_idx || !block_mask) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(perm_q) || !aligned16(perm_k) ||
+      !aligned16(block_idx) || !aligned16(block_mask) ||
+      (block_scores && !aligned16(block_scores)))
+    return BA_ERR_INVALID_ARG;
+  const size_t need = ba_select_workspace_size(batch, heads, seqlen, head_dim, block, kappa,
+                                               sort_mode, sort_window);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return BA_ERR_WORKSPACE;
+  SelectArgs a;
+  a.q = q;
+  a.k = k;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.kappa = kappa;
+  a.beta = beta;
+  a.sort_mode = sort_mode;
+  a.sort_window = sort_window;
+  a.perm_q = perm_q;
+  a.perm_k = perm_k;
+  a.block_idx = block_idx;
+  a.block_mask = block_mask;
+  a.block_scores = block_scores;
+  a.workspace = workspace;
+  return map_cuda(run_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t ba_sparse_attn_workspace_size(int batch, int heads, int seqlen, int head_dim, int block,
+                                     int kappa, int has_perm_q, int has_perm_k) {
+  (void)kappa;
+  if (check_shape(batch, heads, seqlen, head_dim, block) != BA_OK) return 0;
+  return attn_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim,
+                              has_perm_q != 0, has_perm_k != 0);
+}
+
+int ba_sparse_attn(const void *q, const void *k, const void *v, int batch, int heads, int seqlen,
+                   int head_dim, int block, const int32_t *perm_q, const int32_t *perm_k,
+                   const int32_t *block_idx, int kappa, float scale, void *o, float *lse,
+                   void *workspace, size_t workspace_bytes, ba_stream_t stream) {
+  int st = check_shape(batch, heads, seqlen, head_dim, block);
+  if (st != BA_OK) return st;
+  const int n = (seqlen + block - 1) / block;
+  if (kappa < 1 || kappa > n) return BA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !block_idx || !o || !lse) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(block_idx) || (perm_q && !aligned16(perm_q)) || (perm_k && !aligned16(perm_k)))
+    return BA_ERR_INVALID_ARG;
+  const size_t need = ba_sparse_attn_workspace_size(batch, heads, seqlen, head_dim, block, kappa,
+                                                    perm_q != nullptr, perm_k != nullptr);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return BA_ERR_WORKSPACE;
+  AttnArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.perm_q = perm_q;
+  a.perm_k = perm_k;
+  a.block_idx = block_idx;
+  a.kappa = kappa;
+  a.scale = scale;
+  a.o = o;
+  a.lse = lse;
+  a.workspace = workspace;
+  return map_cuda(run_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ba_attn_dense(const void *q, const void *k, const void *v, int batch, int heads, int seqlen,
+                  int head_dim, float scale, void *o, float *lse, ba_stream_t stream) {
+  int st = check_shape(batch, heads, seqlen, head_dim, 128);
+  if (st != BA_OK) return st;
+  if (!isfinite(scale)) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return BA_ERR_INVALID_ARG;
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = 128;
+  a.scale = scale;
+  a.o = o;
+  a.lse = lse;
+  return map_cuda(run_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ba_last_device_error(ba_stream_t stream, uint32_t *detail) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BA_ERR_CUDA;
+  uint32_t word = 0;
+  if (take_attn_error_word(&word) != cudaSuccess) return BA_ERR_CUDA;
+  if (detail) *detail = word;
+  return (word & 1u) ? BA_ERR_DEVICE_TIMEOUT : BA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+// Internal host-side interfaces between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ba {
+
+struct SelectArgs {
+  const void *q, *k;
+  int batch, heads, seqlen, head_dim, block, kappa;
+  float beta;
+  int sort_mode, sort_window;
+  int32_t *perm_q, *perm_k, *block_idx;
+  uint32_t *block_mask;
+  float *block_scores;
+  void *workspace;
+};
+
+struct AttnArgs {
+  const void *q, *k, *v;
+  int batch, heads, seqlen, head_dim, block;
+  const int32_t *perm_q, *perm_k, *block_idx;  // block_idx == nullptr: dense
+  int kappa;
+  float scale;
+  void *o;
+  float *lse;
+  void *workspace;
+};
+
+size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode);
+cudaError_t run_select(const SelectArgs &a, cudaStream_t st);
+
+size_t attn_workspace_bytes(int64_t bh, int L, int D, bool perm_q, bool perm_k);
+cudaError_t run_attention(const AttnArgs &a, cudaStream_t st);
+
+// Reads and clears the attention kernels' device error word (synchronous).
+cudaError_t take_attn_error_word(uint32_t *word);
+
+// Encodes a tiled TMA descriptor (driver entry point resolved at run time).
+cudaError_t encode_tensor_map_3d(void *map_out, const void *base, uint64_t inner, uint64_t rows,
+                                 uint64_t outer, uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace ba

@@ -1,0 +1,163 @@
+/*
+ * ba.h — C ABI of the BA-Att (Block Approximate Sparse Attention) hot path
+ * for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operations follow "Efficient Long-Context Modeling in Diffusion
+ * Language Models via Block Approximate Sparse Attention" (the BA-Att paper):
+ * Algorithm 1 takes Q, K, V, a block size B, a per-query-block budget kappa
+ * and a compensation weight beta, and returns the block mask and the sparse
+ * attention output.  The library adds the per-row log-sum-exp so that results
+ * over disjoint key sets can be merged (the online-softmax merge of the LoSA
+ * summary post, "merge and update").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are dense, row-major, contiguous, on the device, in the layout
+ *    [batch, heads, seqlen, head_dim] ("[b,h,L,d]"); bf16 means IEEE bfloat16
+ *    bit patterns (uint16_t storage).  Every device pointer must be 16-byte
+ *    aligned.  The caller owns every buffer; the library never allocates or
+ *    frees device memory and keeps no state between calls except the device
+ *    error word read by ba_last_device_error().
+ *  - Blocks: N = ceil(L / B) query blocks and N key blocks (self-attention,
+ *    L_q = L_k = L).  When B does not divide L the last block is short.
+ *  - Attention is bidirectional (no causal mask).
+ *  - Every call is asynchronous on `stream` (NULL = legacy default stream):
+ *    host-side checks run first; on any error the call returns a status and
+ *    launches nothing.  A CUDA launch failure returns BA_ERR_CUDA.
+ *  - Supported: head_dim in {64, 128}; block in {64, 128}; 1 <= L;
+ *    b*h*L < 2^31; N <= 4096.  Other values return BA_ERR_UNSUPPORTED.
+ *  - Workspace: each call that needs scratch device memory takes a caller
+ *    buffer of at least the size its *_workspace_size() query returns
+ *    (256-byte aligned); a smaller one returns BA_ERR_WORKSPACE.
+ */
+#ifndef BA_H_
+#define BA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that this header needs no
+ * CUDA header. */
+typedef struct CUstream_st *ba_stream_t;
+
+typedef enum {
+  BA_OK = 0,
+  BA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer */
+  BA_ERR_UNSUPPORTED = 2,    /* valid but not implemented (head_dim, block, N) */
+  BA_ERR_WORKSPACE = 3,      /* workspace smaller than required */
+  BA_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+  BA_ERR_DEVICE_TIMEOUT = 5  /* a kernel gave up on a bounded wait */
+} ba_status;
+
+/* Which token sequences are norm-sorted before blocking (Algorithm 1 steps
+ * 1-2; the ablation of the paper's Table 7: none / SortK / SortQ / both). */
+typedef enum {
+  BA_SORT_NONE = 0,
+  BA_SORT_K = 1,
+  BA_SORT_Q = 2,
+  BA_SORT_QK = 3
+} ba_sort_mode;
+
+/* Human-readable name of a status. Never NULL. */
+const char *ba_status_string(int status);
+
+/* Library version string, e.g. "ba-gb300 0.1 sm_103a". */
+const char *ba_version(void);
+
+/*
+ * Selection stage: BA-Att paper Algorithm 1 steps 1-11 (§3.1 Eq. 2, §3.3
+ * Eq. 9-10, §3.4 Eq. 13-14).
+ *
+ *  1-2. s_i = ||Q_i||, s_j = ||K_j|| (computed as fp32 squared norms, which
+ *       have the same order); a stable non-decreasing sort of each (b,h)
+ *       sequence gives pi_q, pi_k (equal norms keep the lower index first).
+ *       sort_window > 0 sorts each run of sort_window consecutive tokens on
+ *       its own (the algorithm's "(windowed) sort"); 0 sorts the whole
+ *       sequence.  sort_window must be 0 or a multiple of block.
+ *  3-4. Consecutive groups of B sorted tokens form blocks; per block the fp32
+ *       mean and population variance of every feature.
+ *  5-7. l'[gq,gk] = Qbar.Kbar/sqrt(d)
+ *                   + beta/d * sum_t(VarQ_t Kbar_t^2 + VarK_t Qbar_t^2
+ *                                     + VarQ_t VarK_t), in fp32.
+ *  8-11. Per query-block row, the kappa key blocks with the largest l'
+ *       (equal scores: lower key-block index first); the row softmax of
+ *       step 9 preserves this order and is not computed.
+ *
+ * Inputs:  q, k         bf16 [b,h,L,d], device.
+ * Outputs (device, caller-allocated, fully overwritten):
+ *   perm_q, perm_k  int32 [b,h,L]: sorted position -> original token index
+ *                   (the identity when that sequence is not sorted).
+ *   block_idx       int32 [b,h,N,kappa]: selected key blocks, ascending.
+ *   block_mask      uint32 [b,h,N,ceil(N/32)]: bit (gk % 32) of word gk/32
+ *                   is M[gq,gk] (1 = selected); unused high bits are 0.
+ *   block_scores    fp32 [b,h,N,N] l' (may be NULL: not written).
+ * kappa in [1, N]; beta finite (the paper's default is 1).
+ */
+size_t ba_select_workspace_size(int batch, int heads, int seqlen, int head_dim,
+                                int block, int kappa, int sort_mode,
+                                int sort_window);
+
+int ba_select(const void *q, const void *k, int batch, int heads, int seqlen,
+              int head_dim, int block, int kappa, float beta, int sort_mode,
+              int sort_window, int32_t *perm_q, int32_t *perm_k,
+              int32_t *block_idx, uint32_t *block_mask, float *block_scores,
+              void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
+ * Block-sparse attention: BA-Att paper Algorithm 1 step 12 (§2 block-sparse
+ * attention; the masked softmax of SparseD §3.1 Eq. 3-4).  For the token at
+ * sorted query position r (query block g = r / B):
+ *     O[pi_q(r)]   = sum_{j in S(g)} softmax_j(scale * q . k_j) v_j
+ *     lse[pi_q(r)] = ln sum_{j in S(g)} exp(scale * q . k_j)
+ * where S(g) holds every token pi_k(p) whose sorted key position p lies in a
+ * key block listed in block_idx[g].  Results are written in the ORIGINAL
+ * token order (the paper's remap by pi_q^-1).
+ *
+ * q, k, v     bf16 [b,h,L,d], device.
+ * perm_q, perm_k  int32 [b,h,L] as produced by ba_select, or NULL for the
+ *             identity.  Each must be a permutation of 0..L-1 per (b,h)
+ *             (not checked; an invalid one gives undefined results).
+ * block_idx   int32 [b,h,N,kappa], strictly ascending ids < N per row (not
+ *             checked on the device).
+ * scale       logit scale; <= 0 selects 1/sqrt(d).
+ * o           bf16 [b,h,L,d] output;  lse  fp32 [b,h,L] output (natural log).
+ * Uses tcgen05 tensor-core MMAs (bf16 in, fp32 accumulate in tensor memory).
+ */
+size_t ba_sparse_attn_workspace_size(int batch, int heads, int seqlen,
+                                     int head_dim, int block, int kappa,
+                                     int has_perm_q, int has_perm_k);
+
+int ba_sparse_attn(const void *q, const void *k, const void *v, int batch,
+                   int heads, int seqlen, int head_dim, int block,
+                   const int32_t *perm_q, const int32_t *perm_k,
+                   const int32_t *block_idx, int kappa, float scale, void *o,
+                   float *lse, void *workspace, size_t workspace_bytes,
+                   ba_stream_t stream);
+
+/*
+ * Dense attention with the same kernel (every key block of every row, no
+ * permutation): softmax(scale * Q K^T) V and its row LSE — the BA-Att
+ * paper's Eq. 1, the dense reference its speedups are measured against.
+ * Arguments as in ba_sparse_attn.  Needs no workspace.
+ */
+int ba_attn_dense(const void *q, const void *k, const void *v, int batch,
+                  int heads, int seqlen, int head_dim, float scale, void *o,
+                  float *lse, ba_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word that
+ * kernels set when a bounded wait gives up.  Returns BA_OK,
+ * BA_ERR_DEVICE_TIMEOUT or BA_ERR_CUDA.  `detail` (may be NULL) receives the
+ * raw word: bit 0 = timeout, bits 8-15 = the first site that gave up.
+ */
+int ba_last_device_error(ba_stream_t stream, uint32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BA_H_ */

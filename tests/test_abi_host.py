@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every function include/ba.h declares, and rejects bad
+arguments with the documented status before touching the device."""
+
+import ctypes
+
+import pytest
+
+import block_sparse_bidirectional_gb300 as bsb
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+
+# Plausible-looking device addresses: 256-byte aligned, never dereferenced
+# because every call below fails its host checks first.
+P = ctypes.c_void_p(0x10000000)
+P2 = ctypes.c_void_p(0x20000000)
+MIS = ctypes.c_void_p(0x10000004)  # not 16-byte aligned
+
+
+def test_header_declares_the_documented_calls():
+    names = set(bsb.header_functions())
+    for n in ("ba_select", "ba_sparse_attn", "ba_attn_dense", "ba_select_workspace_size",
+              "ba_sparse_attn_workspace_size", "ba_status_string", "ba_version",
+              "ba_last_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_header_function():
+    lib = bsb.load()
+    for name in bsb.header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version():
+    lib = bsb.load()
+    assert lib.ba_status_string(0) == b"BA_OK"
+    for s in range(1, 6):
+        assert lib.ba_status_string(s).startswith(b"BA_ERR_")
+    assert lib.ba_status_string(99) == b"BA_ERR_UNKNOWN"
+    assert b"sm_103a" in lib.ba_version()
+
+
+def test_workspace_sizes():
+    lib = bsb.load()
+    # no sort: no key buffers; stats (a, b) + scores scratch
+    b, h, L, d, B = 1, 32, 65536, 128, 128
+    N = L // B
+    aug = b * h * N * 3 * d * 4
+    sc = b * h * N * N * 4
+    keys = 2 * b * h * L * 8
+    assert lib.ba_select_workspace_size(b, h, L, d, B, 256, 0, 0) == 2 * aug + sc
+    assert lib.ba_select_workspace_size(b, h, L, d, B, 256, 3, 0) == 2 * keys + 2 * aug + sc
+    t = b * h * L * d * 2
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 0) == 0
+    # unsupported shapes report 0
+    assert lib.ba_select_workspace_size(1, 1, 1024, 96, 64, 8, 3, 0) == 0
+    assert lib.ba_select_workspace_size(1, 1, 1024, 64, 32, 8, 3, 0) == 0
+
+
+def _select(lib, **kw):
+    a = dict(q=P, k=P, b=1, h=1, L=1024, d=64, B=64, kappa=8, beta=1.0, mode=3, win=0,
+             pq=P2, pk=P2, idx=P2, mask=P2, scores=None, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ba_select(a["q"], a["k"], a["b"], a["h"], a["L"], a["d"], a["B"], a["kappa"],
+                         a["beta"], a["mode"], a["win"], a["pq"], a["pk"], a["idx"], a["mask"],
+                         a["scores"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), INVALID),
+    (dict(k=MIS), INVALID),
+    (dict(idx=None), INVALID),
+    (dict(mask=MIS), INVALID),
+    (dict(kappa=0), INVALID),
+    (dict(kappa=17), INVALID),
+    (dict(mode=4), INVALID),
+    (dict(win=100), INVALID),
+    (dict(beta=float("nan")), INVALID),
+    (dict(L=0), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(B=32), UNSUPPORTED),
+    (dict(L=64 * 4097, kappa=8), UNSUPPORTED),
+    (dict(ws_bytes=1024), WORKSPACE),
+    (dict(ws=None), WORKSPACE),
+    (dict(ws=ctypes.c_void_p(0x10000010)), WORKSPACE),
+])
+def test_select_rejects(kw, status):
+    assert _select(bsb.load(), **kw) == status
+
+
+def _attn(lib, **kw):
+    a = dict(q=P, k=P, v=P, b=1, h=1, L=1024, d=64, B=64, pq=P2, pk=P2, idx=P2, kappa=8, scale=0.0,
+             o=P, lse=P, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ba_sparse_attn(a["q"], a["k"], a["v"], a["b"], a["h"], a["L"], a["d"], a["B"],
+                              a["pq"], a["pk"], a["idx"], a["kappa"], a["scale"], a["o"], a["lse"],
+                              a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(v=None), INVALID),
+    (dict(o=MIS), INVALID),
+    (dict(pq=MIS), INVALID),
+    (dict(kappa=0), INVALID),
+    (dict(kappa=17), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(d=80), UNSUPPORTED),
+    (dict(B=256), UNSUPPORTED),
+    (dict(ws_bytes=16), WORKSPACE),
+])
+def test_sparse_attn_rejects(kw, status):
+    assert _attn(bsb.load(), **kw) == status
+
+
+def test_dense_rejects():
+    lib = bsb.load()
+    assert lib.ba_attn_dense(None, P, P, 1, 1, 128, 64, 0.0, P, P, None) == INVALID
+    assert lib.ba_attn_dense(P, P, P, 1, 1, 128, 72, 0.0, P, P, None) == UNSUPPORTED
+    assert lib.ba_attn_dense(P, P, P, 1, 1, 0, 64, 0.0, P, P, None) == INVALID
+    assert lib.ba_attn_dense(P, P, P, 1, 1, 128, 64, 0.0, MIS, P, None) == INVALID
+
+
+def test_no_cpu_path():
+    """The binding refuses CPU tensors instead of computing anything on the host."""
+    import torch
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        bsb.ba_attn_dense(q, q, q)
+    with pytest.raises(ValueError):
+        bsb.ba_select(q, q, 64, 1)
