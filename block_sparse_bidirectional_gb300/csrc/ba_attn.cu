@@ -55,6 +55,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 constexpr int next_pow2_cols(int x) {
   int c = 32;
   while (c < x) c <<= 1;
@@ -297,7 +300,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int row_sorted = tile * kTileM + r;
     const bool row_valid = row_sorted < p.L;
     const int my_g = r / BK;
-    float m_used = -INFINITY, l = 0.f;
+    // l: sum of the exact fp32 weights (for the LSE); lr: sum of the
+    // bf16-rounded weights the PV product consumes (normalises O, so O is an
+    // exact convex combination of V rows up to fp32 accumulation)
+    float m_used = -INFINITY, l = 0.f, lr = 0.f;
     bool ok = true;
     for (int j = 0; j < n_iter; ++j) {
       const uint32_t e = p.dense ? (static_cast<uint32_t>(j) | (3u << 12)) : list[j];
@@ -329,6 +335,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (need) {
         alpha = resc ? fast_exp2(m_used - m_cand) : 0.f;
         l *= alpha;
+        lr *= alpha;
         m_used = m_cand;
       }
       if (__any_sync(0xffffffffu, resc)) {
@@ -359,6 +366,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         w.y = pack_bf16(x[2], x[3]);
         w.z = pack_bf16(x[4], x[5]);
         w.w = pack_bf16(x[6], x[7]);
+        lr += bf16_lo(w.x) + bf16_hi(w.x) + bf16_lo(w.y) + bf16_hi(w.y) + bf16_lo(w.z) +
+             bf16_hi(w.z) + bf16_lo(w.w) + bf16_hi(w.w);
         const int chunk = u16 / 8, u = u16 % 8;
         *reinterpret_cast<uint4 *>(sP + chunk * kTileM * 128 + r * 128 + ((u ^ (r & 7)) << 4)) = w;
       }
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int64_t orig = row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted]
                                                  : row_sorted)
                                      : 0;
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
       uint4 *orow = reinterpret_cast<uint4 *>(p.o + (static_cast<int64_t>(bh) * p.L + orig) * D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
