@@ -19,7 +19,7 @@ import re
 
 from . import _build
 
-__all__ = ["load", "ba_select", "ba_select_into", "ba_sparse_attn", "ba_sparse_attn_into",
+__all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_sparse_attn", "ba_sparse_attn_into",
            "ba_attn_dense", "ba_attn_dense_into", "last_device_error", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
            "sparse_attn_workspace_size", "header_functions", "LIB_PATH"]
@@ -42,6 +42,8 @@ _SIGS = {
                        + [_c_void_p] * 3 + [_c_size, _c_void_p]),
     "ba_attn_dense": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [_c_float] + [_c_void_p] * 3),
     "ba_last_device_error": (_c_int, [_c_void_p, _c_u32p]),
+    "ba_select_noalloc": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int]
+                          + [_c_void_p] * 5 + [_c_void_p]),
 }
 
 _lib = None
@@ -131,6 +133,19 @@ def ba_select_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, per
                        _ptr(perm_q), _ptr(perm_k), _ptr(block_idx), _ptr(block_mask),
                        _ptr(block_scores), _ptr(workspace), ws_bytes, _stream(q.device))
     _check(st, "ba_select")
+
+
+def ba_select_noalloc_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, perm_k,
+                           block_idx, block_mask, block_scores):
+    """ba_select through the library's built-in scratch array (for callers that
+    cannot allocate device memory); writes caller-allocated outputs."""
+    lib = load()
+    _need_cuda(q, k, perm_q, perm_k, block_idx, block_mask, block_scores)
+    b, h, L, d = q.shape
+    st = lib.ba_select_noalloc(_ptr(q), _ptr(k), b, h, L, d, block, kappa, float(beta), sort_mode,
+                               sort_window, _ptr(perm_q), _ptr(perm_k), _ptr(block_idx),
+                               _ptr(block_mask), _ptr(block_scores), _stream(q.device))
+    _check(st, "ba_select_noalloc")
 
 
 def ba_select(q, k, block, kappa, beta=1.0, sort_mode=SORT_QK, sort_window=0, return_scores=False,

@@ -17,7 +17,8 @@
  *    bit patterns (uint16_t storage).  Every device pointer must be 16-byte
  *    aligned.  The caller owns every buffer; the library never allocates or
  *    frees device memory and keeps no state between calls except the device
- *    error word read by ba_last_device_error().
+ *    error word read by ba_last_device_error() and the fixed scratch array
+ *    of ba_select_noalloc().
  *  - Blocks: N = ceil(L / B) query blocks and N key blocks (self-attention,
  *    L_q = L_k = L).  When B does not divide L the last block is short.
  *  - Attention is bidirectional (no causal mask).
@@ -106,6 +107,41 @@ int ba_select(const void *q, const void *k, int batch, int heads, int seqlen,
               int sort_window, int32_t *perm_q, int32_t *perm_k,
               int32_t *block_idx, uint32_t *block_mask, float *block_scores,
               void *workspace, size_t workspace_bytes, ba_stream_t stream);
+
+/*
+ * ba_select without a workspace argument, for callers that cannot allocate
+ * device memory when they select: for example a serving engine that reserves
+ * the whole GPU heap for its own pool at start-up and allows no cudaMalloc
+ * afterwards, or a plugin running inside a framework whose allocator it
+ * cannot reach.  The paper has no counterpart to this call; it exists for
+ * such deployments only.
+ *
+ * Same arguments, outputs and checks as ba_select, minus workspace and
+ * workspace_bytes.  The scratch memory is a fixed array of
+ * BA_SELECT_STATIC_SCRATCH_BYTES compiled into the library; every GPU that
+ * loads the library holds that much device memory until the process exits.
+ *  - Sizes whose ba_select_workspace_size() exceeds
+ *    BA_SELECT_STATIC_SCRATCH_BYTES are rejected with BA_ERR_WORKSPACE before
+ *    anything is launched (32 heads of L = 8192, d = 128, B = 64 fit).
+ *  - The first call on a device looks up that device's copy of the array
+ *    (cudaGetSymbolAddress with the device current) and caches it; make that
+ *    first call before any stream capture begins.  The current device must be
+ *    the device of `stream`.
+ *  - The library allocates and frees nothing in this call.
+ *  - Every call on a device shares the one array: calls whose work overlaps on
+ *    the GPU (different streams, or different host threads) race on it and
+ *    give undefined results.  Serialise them, e.g. on one stream.  Nothing has
+ *    to be cleared between calls: every scratch element is written before it
+ *    is read.
+ */
+#define BA_SELECT_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+int ba_select_noalloc(const void *q, const void *k, int batch, int heads,
+                      int seqlen, int head_dim, int block, int kappa,
+                      float beta, int sort_mode, int sort_window,
+                      int32_t *perm_q, int32_t *perm_k, int32_t *block_idx,
+                      uint32_t *block_mask, float *block_scores,
+                      ba_stream_t stream);
 
 /*
  * Block-sparse attention: BA-Att paper Algorithm 1 step 12 (§2 block-sparse
