@@ -38,9 +38,11 @@
 
 namespace ba {
 
-constexpr int kTileM = 128;
-constexpr int kAttnThreads = 256;
-constexpr int kStages = 2;
+constexpr int kTileM = 128;          // query rows per tile (TMEM lanes)
+constexpr int kTiles = 2;            // query tiles per CTA (ping-pong)
+constexpr int kAttnThreads = 384;    // 12 warps
+constexpr int kRegsLow = 72;         // warps 0-3 after setmaxnreg.dec
+constexpr int kRegsHigh = 216;       // warps 4-11 after setmaxnreg.inc (4*32*72 + 8*32*216 = 384*168)
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxBlocks = 4096;
 
@@ -63,37 +65,38 @@ constexpr int next_pow2_cols(int x) {
   while (c < x) c <<= 1;
   return c;
 }
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 template <int D, int BK>
 struct AttnLayout {
-  static constexpr int kQBytes = kTileM * D * 2;
-  static constexpr int kKVBytes = BK * D * 2;
-  static constexpr int kPBytes = kTileM * BK * 2;
+  static constexpr int kG = kTileM / BK;               // query blocks per tile
+  static constexpr int kQBytes = kTileM * D * 2;       // one Q tile
+  static constexpr int kSlotBytes = BK * D * 2;        // one K or V block
+  static constexpr int kListBytes = (kG > 1) ? kTiles * kMaxBlocks * 2 : 0;
+  static constexpr int kBarBytes = 512;
+  static constexpr int kMaxDyn = 227 * 1024;
+  static constexpr int kSlots =
+      cmin(8, (kMaxDyn - 1024 - kBarBytes - kListBytes - kTiles * kQBytes) / kSlotBytes);
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffP = kOffV + kStages * kKVBytes;
-  static constexpr int kOffList = kOffP + kPBytes;
-  static constexpr int kOffBitmap = kOffList + kMaxBlocks * 2;
-  static constexpr int kOffBar = kOffBitmap + 2 * (kMaxBlocks / 32) * 4;
-  static constexpr int kNumBars = 1 + 4 * kStages + 2 + 1 + 1 + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kBytes = kOffMisc + 64;
-  static constexpr int kTmemCols = next_pow2_cols(2 * BK + D);
-  // Shared memory is padded so that no more CTAs fit on an SM than its 512
-  // tensor-memory columns can hold (an allocation would otherwise stall).
+  static constexpr int kOffSlots = kOffQ + kTiles * kQBytes;
+  static constexpr int kOffList = kOffSlots + kSlots * kSlotBytes;
+  static constexpr int kOffBar = kOffList + kListBytes;
+  static constexpr int kBytes = kOffBar + kBarBytes;
+  static constexpr int kTmemCols = next_pow2_cols(kTiles * (BK + D));
+  // No more CTAs may share an SM than its 512 tensor-memory columns can hold.
   static constexpr int kMaxCtasByTmem = 512 / kTmemCols;
   static constexpr int kMinAlloc = (228 * 1024) / (kMaxCtasByTmem + 1) + 1024;
   static constexpr int kAlloc = (kBytes + 1024 > kMinAlloc) ? kBytes + 1024 : kMinAlloc;
+  static_assert(kSlots >= 3, "shared memory ring too small");
   static_assert(kTmemCols <= 512, "tensor memory budget");
-  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+  static_assert(kAlloc <= kMaxDyn, "shared memory budget");
 };
 
 struct AttnParams {
   int L;          // tokens per sequence
   int N;          // key blocks (and query blocks) of size BK
   int kappa;      // list length per query block (unused when dense)
-  int dense;      // 1: every key block, no list
+  int n_tiles;    // 128-row query tiles per sequence
   const int32_t *block_idx;
   const int32_t *perm_q;  // sorted query position -> original row (nullable)
   __nv_bfloat16 *o;
@@ -101,53 +104,58 @@ struct AttnParams {
   float scale_log2;       // scale * log2(e)
 };
 
-template <int D, int BK>
+// A key-block entry: bits 0-11 block id, bit 12+g set when query block g of
+// the tile selected it.
+template <int G, bool kDense>
+__device__ __forceinline__ uint32_t entry_at(const AttnParams &p, const uint16_t *list,
+                                             const int32_t *idx, int j) {
+  if (kDense) return static_cast<uint32_t>(j) | (3u << 12);
+  if (G == 1) return static_cast<uint32_t>(min(max(__ldg(idx + j), 0), p.N - 1)) | (1u << 12);
+  return list[j];
+}
+
+template <int D, int BK, bool kDense>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Lay = AttnLayout<D, BK>;
-  constexpr int G = kTileM / BK;  // query blocks per tile
+  constexpr int G = Lay::kG;
+  constexpr int S = Lay::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sQ = smem + Lay::kOffQ;
-  uint8_t *sK = smem + Lay::kOffK;
-  uint8_t *sV = smem + Lay::kOffV;
-  uint8_t *sP = smem + Lay::kOffP;
-  uint16_t *list = reinterpret_cast<uint16_t *>(smem + Lay::kOffList);
-  uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + Lay::kOffBitmap);
+  uint8_t *sSlot = smem + Lay::kOffSlots;
+  uint16_t *lists = reinterpret_cast<uint16_t *>(smem + Lay::kOffList);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
   uint64_t *q_full = bars;
-  uint64_t *k_full = bars + 1;
-  uint64_t *k_empty = k_full + kStages;
-  uint64_t *v_full = k_empty + kStages;
-  uint64_t *v_empty = v_full + kStages;
-  uint64_t *s_full = v_empty + kStages;
-  uint64_t *p_full = s_full + 2;
-  uint64_t *o_done = p_full + 1;
-  uint64_t *drain = o_done + 1;
-  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + Lay::kOffMisc);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(&misc[2]);
+  uint64_t *slot_full = bars + 1;
+  uint64_t *slot_empty = slot_full + S;
+  uint64_t *s_full = slot_empty + S;   // [kTiles]
+  uint64_t *p_full = s_full + kTiles;  // [kTiles]
+  uint64_t *o_done = p_full + kTiles;  // [kTiles]
+  uint64_t *drain = o_done + kTiles;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(drain + 1);  // tmem, n0, n1, abort
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(&misc[3]);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int tile = blockIdx.x;
+  const int tile0 = blockIdx.x * kTiles;
   const int bh = blockIdx.y;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&slot_full[s], 1);
+      mbar_init(&slot_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
+    for (int t = 0; t < kTiles; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], kTileM);
+      mbar_init(&o_done[t], 1);
+    }
     mbar_init(drain, 1);
-    misc[1] = 0;
-    misc[2] = 0;
+    misc[1] = misc[2] = 0;
+    misc[3] = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -156,188 +164,239 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_before();
   }
 
-  // ---- the key-block list of this tile ------------------------------------
-  if (!p.dense) {
-    if (G == 1) {
-      const int32_t *src = p.block_idx + (static_cast<int64_t>(bh) * p.N + tile) * p.kappa;
-      for (int i = threadIdx.x; i < p.kappa; i += kAttnThreads)
-        list[i] = static_cast<uint16_t>(min(max(src[i], 0), p.N - 1) | (1 << 12));
-      if (threadIdx.x == 0) misc[1] = p.kappa;
-    } else {
-      const int nwords = (p.N + 31) / 32;
-      for (int i = threadIdx.x; i < 2 * (kMaxBlocks / 32); i += kAttnThreads) bitmap[i] = 0u;
-      __syncthreads();
+  // ---- per-tile key-block lists ------------------------------------------
+  if (kDense || G == 1) {
+    if (threadIdx.x < kTiles) {
+      const int tile = tile0 + threadIdx.x;
+      misc[1 + threadIdx.x] = (tile < p.n_tiles) ? (kDense ? p.N : p.kappa) : 0;
+    }
+  } else {
+    // G == 2: per tile, the union of its two query blocks' lists, ascending,
+    // each entry tagged with which of the two selected it.
+    constexpr int kWords = kMaxBlocks / 32;
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(sSlot);  // scratch, before any load
+    const int nwords = (p.N + 31) / 32;
+    for (int i = threadIdx.x; i < kTiles * G * kWords; i += kAttnThreads) bitmap[i] = 0u;
+    __syncthreads();
+    for (int t = 0; t < kTiles; ++t)
       for (int g = 0; g < G; ++g) {
-        const int gq = tile * G + g;
-        if (gq >= p.N) break;
+        const int gq = (tile0 + t) * G + g;
+        if (gq >= p.N) continue;
         const int32_t *src = p.block_idx + (static_cast<int64_t>(bh) * p.N + gq) * p.kappa;
         for (int i = threadIdx.x; i < p.kappa; i += kAttnThreads) {
           const int blk = src[i];
           if (blk < 0 || blk >= p.N) continue;  // ids are not validated on the host
-          atomicOr(&bitmap[g * (kMaxBlocks / 32) + (blk >> 5)], 1u << (blk & 31));
+          atomicOr(&bitmap[(t * G + g) * kWords + (blk >> 5)], 1u << (blk & 31));
         }
       }
-      __syncthreads();
-      if (warp == 0) {
-        int base = 0;
-        for (int w0 = 0; w0 < nwords; w0 += 32) {
-          const int w = w0 + lane;
-          const uint32_t m0 = (w < nwords) ? bitmap[w] : 0u;
-          const uint32_t m1 = (w < nwords) ? bitmap[(kMaxBlocks / 32) + w] : 0u;
-          uint32_t u = m0 | m1;
-          const int cnt = __popc(u);
-          int incl = cnt;
+    __syncthreads();
+    if (warp < kTiles) {
+      const int t = warp;
+      uint16_t *list = lists + t * kMaxBlocks;
+      int base = 0;
+      for (int w0 = 0; w0 < nwords; w0 += 32) {
+        const int w = w0 + lane;
+        const uint32_t m0 = (w < nwords) ? bitmap[(t * G + 0) * kWords + w] : 0u;
+        const uint32_t m1 = (w < nwords) ? bitmap[(t * G + 1) * kWords + w] : 0u;
+        uint32_t u = m0 | m1;
+        const int cnt = __popc(u);
+        int incl = cnt;
 #pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += t;
-          }
-          int pos = base + incl - cnt;
-          while (u) {
-            const int b = __ffs(u) - 1;
-            u &= u - 1;
-            const uint32_t sel = ((m0 >> b) & 1u) | (((m1 >> b) & 1u) << 1);
-            list[pos++] = static_cast<uint16_t>((w * 32 + b) | (sel << 12));
-          }
-          base += __shfl_sync(0xffffffffu, incl, 31);
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
         }
-        if (lane == 0) misc[1] = base;
+        int pos = base + incl - cnt;
+        while (u) {
+          const int b = __ffs(u) - 1;
+          u &= u - 1;
+          const uint32_t sel = ((m0 >> b) & 1u) | (((m1 >> b) & 1u) << 1);
+          list[pos++] = static_cast<uint16_t>((w * 32 + b) | (sel << 12));
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
       }
+      if (lane == 0) misc[1 + t] = base;
     }
+    // the bitmap scratch is overwritten by TMA (async proxy) later
+    fence_proxy_async_smem();
   }
   __syncthreads();
   tc_fence_after();
-  const int n_iter = p.dense ? p.N : static_cast<int>(misc[1]);
   const uint32_t tmem = misc[0];
+  const int n_t[kTiles] = {static_cast<int>(misc[1]), static_cast<int>(misc[2])};
+  const int nmax = max(n_t[0], n_t[1]);
+  // dense: both tiles walk the same blocks, so every K/V load serves both
+  const bool shared = kDense && n_t[1] > 0;
+  const int32_t *idx_t[kTiles];
+  for (int t = 0; t < kTiles; ++t)
+    idx_t[t] = p.block_idx + (static_cast<int64_t>(bh) * p.N + (tile0 + t)) * p.kappa;
 
-  if (warp == 0) {
-    // ===================== TMA producer =====================================
-    if (lane == 0) {
+  if (warp < 4) {
+    reg_dealloc<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ===================== TMA producer ===================================
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      int nk[kStages] = {}, nv[kStages] = {};
-      mbar_arrive_expect_tx(q_full, Lay::kQBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(sQ + c * kTileM * 128, &tmQ, q_full, c * 64, tile * kTileM, bh);
-      for (int j = 0; j < n_iter; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = (j / kStages) & 1;
-        const int blk = p.dense ? j : (list[j] & 0xFFF);
-        if (j >= kStages && !mbar_wait(&k_empty[s], ph ^ 1u, kSiteKEmpty, abort_flag)) break;
-        mbar_arrive_expect_tx(&k_full[s], Lay::kKVBytes);
+      uint32_t qbytes = 0;
+      for (int t = 0; t < kTiles; ++t) qbytes += n_t[t] > 0 ? Lay::kQBytes : 0;
+      mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < kTiles; ++t) {
+        if (n_t[t] == 0) continue;
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sK + s * Lay::kKVBytes + c * BK * 128, &tmK, &k_full[s], c * 64, blk * BK,
-                      bh);
-        ++nk[s];
-        if (j >= kStages && !mbar_wait(&v_empty[s], ph ^ 1u, kSiteVEmpty, abort_flag)) break;
-        mbar_arrive_expect_tx(&v_full[s], Lay::kKVBytes);
+          tma_load_3d(sQ + t * Lay::kQBytes + c * kTileM * 128, &tmQ, q_full, c * 64,
+                      (tile0 + t) * kTileM, bh);
+      }
+      int issued = 0;
+      auto load = [&](bool is_v, int t, int j) -> bool {
+        const int blk = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j) & 0xFFF;
+        const int s = issued % S;
+        if (issued >= S && !mbar_wait(&slot_empty[s], ((issued / S) & 1) ^ 1u, kSiteKEmpty, abort_flag))
+          return false;
+        mbar_arrive_expect_tx(&slot_full[s], Lay::kSlotBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sV + s * Lay::kKVBytes + c * BK * 128, &tmV, &v_full[s], c * 64, blk * BK,
-                      bh);
-        ++nv[s];
-      }
-      // drain: the last copy issued on each barrier has landed
-      mbar_wait_drain(q_full, 0);
-      for (int s = 0; s < kStages; ++s) {
-        if (nk[s]) mbar_wait_drain(&k_full[s], (nk[s] - 1) & 1);
-        if (nv[s]) mbar_wait_drain(&v_full[s], (nv[s] - 1) & 1);
-      }
-    }
-  } else if (warp == 1) {
-    // ===================== MMA issuer =======================================
-    if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(kTileM, BK, 0, 0);
-      const uint32_t idO = idesc_bf16_f32(kTileM, D, 0, 1);
-      const uint32_t tS0 = tmem, tS1 = tmem + BK, tO = tmem + 2 * BK;
-      const uint32_t q_addr = smem_u32(sQ), k_addr = smem_u32(sK);
-      const uint32_t v_addr = smem_u32(sV), p_addr = smem_u32(sP);
-      bool ok = mbar_wait(q_full, 0, kSiteQFull, abort_flag);
-      tc_fence_after();
-      auto issue_s = [&](int j) -> bool {
-        const int s = j % kStages;
-        if (!mbar_wait(&k_full[s], (j / kStages) & 1, kSiteKFull, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t dst = (j & 1) ? tS1 : tS0;
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(q_addr + (ks / 4) * kTileM * 128 + (ks % 4) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(
-              k_addr + s * Lay::kKVBytes + (ks / 4) * BK * 128 + (ks % 4) * 32, 16, 1024);
-          mma_bf16_ss(dst, a, b, idS, ks > 0 ? 1u : 0u);
-        }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&k_empty[s]);
+          tma_load_3d(sSlot + s * Lay::kSlotBytes + c * BK * 128, is_v ? &tmV : &tmK, &slot_full[s],
+                      c * 64, blk * BK, bh);
+        ++issued;
         return true;
       };
-      if (ok && n_iter > 0) ok = issue_s(0);
-      for (int j = 0; ok && j < n_iter; ++j) {
-        if (j + 1 < n_iter && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(p_full, j & 1, kSitePFull, abort_flag))) break;
-        const int s = j % kStages;
-        if (!(ok = mbar_wait(&v_full[s], (j / kStages) & 1, kSiteVFull, abort_flag))) break;
+      // the same operand order in which the MMA thread consumes the slots
+      bool ok = true;
+      for (int t = 0; ok && t < kTiles; ++t)
+        if (n_t[t] > 0 && !(shared && t == 1)) ok = load(false, t, 0);
+      for (int j = 0; ok && j < nmax; ++j)
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (j >= n_t[t] || (shared && t == 1)) continue;
+          ok = load(true, t, j);
+          if (ok && j + 1 < n_t[t]) ok = load(false, t, j + 1);
+        }
+      // drain: the last copy issued into each slot has landed
+      mbar_wait_drain(q_full, 0);
+      for (int s = 0; s < S && s < issued; ++s) {
+        const int last = s + S * ((issued - 1 - s) / S);
+        mbar_wait_drain(&slot_full[s], (last / S) & 1);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ===================== MMA issuer =====================================
+      const uint32_t idS = idesc_bf16_f32(kTileM, BK, 0, 0);
+      const uint32_t idO = idesc_bf16_f32(kTileM, D, 0, 1);
+      const uint32_t q_addr = smem_u32(sQ), slot_addr = smem_u32(sSlot);
+      int consumed = 0;
+      bool ok = mbar_wait(q_full, 0, kSiteQFull, abort_flag);
+      tc_fence_after();
+      auto take = [&](int &slot) -> bool {
+        slot = consumed % S;
+        if (!mbar_wait(&slot_full[slot], (consumed / S) & 1, kSiteKFull, abort_flag)) return false;
         tc_fence_after();
+        ++consumed;
+        return true;
+      };
+      auto mma_s = [&](int t, int slot) {
+        const uint32_t qa = q_addr + t * Lay::kQBytes;
+        const uint32_t ka = slot_addr + slot * Lay::kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint64_t a = smem_desc_sw128(qa + (ks / 4) * kTileM * 128 + (ks % 4) * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(ka + (ks / 4) * BK * 128 + (ks % 4) * 32, 16, 1024);
+          mma_bf16_ss(tmem + t * BK, a, b, idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[t]);
+      };
+      auto mma_pv = [&](int t, int slot, int j) {
+        const uint32_t va = slot_addr + slot * Lay::kSlotBytes;
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(p_addr + (ks / 4) * kTileM * 128 + (ks % 4) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(v_addr + s * Lay::kKVBytes + ks * 16 * 128, BK * 128, 1024);
-          mma_bf16_ss(tO, a, b, idO, (j > 0 || ks > 0) ? 1u : 0u);
+          const uint64_t b = smem_desc_sw128(va + ks * 16 * 128, BK * 128, 1024);
+          mma_bf16_ts(tmem + kTiles * BK + t * D, tmem + t * BK + ks * 8, b, idO,
+                      (j > 0 || ks > 0) ? 1u : 0u);
         }
-        mma_commit(o_done);
-        mma_commit(&v_empty[s]);
+      };
+      int slot_k0 = 0, slot_v0 = 0;  // dense: slots loaded for tile 0, reused by tile 1
+      for (int t = 0; ok && t < kTiles; ++t) {
+        if (n_t[t] == 0) continue;
+        int sl = slot_k0;
+        if (!(shared && t == 1) && !(ok = take(sl))) break;
+        mma_s(t, sl);
+        if (!shared || t == 1) mma_commit(&slot_empty[sl]);
+        else slot_k0 = sl;
+      }
+      for (int j = 0; ok && j < nmax; ++j) {
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (j >= n_t[t]) continue;
+          if (!(ok = mbar_wait(&p_full[t], j & 1, kSitePFull, abort_flag))) break;
+          tc_fence_after();
+          int sv = slot_v0;
+          if (!(shared && t == 1) && !(ok = take(sv))) break;
+          mma_pv(t, sv, j);
+          if (j + 1 == n_t[t]) mma_commit(&o_done[t]);
+          if (!shared || t == 1) mma_commit(&slot_empty[sv]);
+          else slot_v0 = sv;
+          if (j + 1 < n_t[t]) {
+            int sk = slot_k0;
+            if (!(shared && t == 1) && !(ok = take(sk))) break;
+            mma_s(t, sk);
+            if (!shared || t == 1) mma_commit(&slot_empty[sk]);
+            else slot_k0 = sk;
+          }
+        }
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
     }
-  } else if (warp >= 4) {
-    // ===================== softmax + epilogue ===============================
-    const int r = threadIdx.x - 128;
+  } else {
+    reg_alloc<kRegsHigh>();
+    // ===================== softmax + epilogue, one warpgroup per tile =======
+    const int t = (warp - 4) >> 2;
+    const int r = threadIdx.x - 128 * (t + 1);
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS0 = tmem + lane_base, tS1 = tS0 + BK, tO = tS0 + 2 * BK;
-    const int row_sorted = tile * kTileM + r;
+    const uint32_t tS = tmem + lane_base + t * BK;
+    const uint32_t tO = tmem + lane_base + kTiles * BK + t * D;
+    const int row_sorted = (tile0 + t) * kTileM + r;
     const bool row_valid = row_sorted < p.L;
     const int my_g = r / BK;
-    // l: sum of the exact fp32 weights (for the LSE); lr: sum of the
-    // bf16-rounded weights the PV product consumes (normalises O, so O is an
-    // exact convex combination of V rows up to fp32 accumulation)
-    float m_used = -INFINITY, l = 0.f, lr = 0.f;
+    const float cl = p.scale_log2;
+    const uint64_t cl2 = f2_pack(cl, cl);
+    float m = -INFINITY;
+    uint64_t l2 = f2_pack(0.f, 0.f);   // exact weights: for the LSE
+    uint64_t lr2 = f2_pack(0.f, 0.f);  // bf16-rounded weights: normalise O
     bool ok = true;
-    for (int j = 0; j < n_iter; ++j) {
-      const uint32_t e = p.dense ? (static_cast<uint32_t>(j) | (3u << 12)) : list[j];
+    const int n = n_t[t];
+    for (int j = 0; j < n; ++j) {
+      const uint32_t e = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j);
       const int blk = e & 0xFFF;
-      const bool use = row_valid && ((e >> (12 + my_g)) & 1u);
-      ok = mbar_wait(&s_full[j & 1], (j >> 1) & 1, kSiteSFull, abort_flag);
+      const bool sel = (e >> (12 + my_g)) & 1u;
+      const int valid_cols = min(BK, p.L - blk * BK);
+      ok = mbar_wait(&s_full[t], j & 1, kSiteSFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float sv[BK];
 #pragma unroll
-      for (int c = 0; c < BK / 32; ++c) tmem_ld32(((j & 1) ? tS1 : tS0) + c * 32, sv + c * 32);
+      for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + c * 32, sv + c * 32);
       tmem_wait_ld();
-      const int valid_cols = min(BK, p.L - blk * BK);
-      float mx = -INFINITY;
-      if (use) {
+      if (!sel || valid_cols < BK) {
 #pragma unroll
         for (int c = 0; c < BK; ++c)
-          if (c < valid_cols) mx = fmaxf(mx, sv[c]);
+          if (!sel || c >= valid_cols) sv[c] = -INFINITY;
       }
-      const float m_cand = fmaxf(m_used, mx * p.scale_log2);
-      if (j > 0) {
-        ok = mbar_wait(o_done, (j - 1) & 1, kSiteODone, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
-      const bool need = m_cand > m_used + kRescaleLog2;
-      const bool resc = need && (m_used != -INFINITY);
+      float mx = sv[0];
+#pragma unroll
+      for (int c = 1; c + 1 < BK; c += 2) mx = max3f(mx, sv[c], sv[c + 1]);
+      mx = fmaxf(mx, sv[BK - 1]);
+      const float m_new = fmaxf(m, mx * cl);
+      const bool need = m_new > m + kRescaleLog2;
+      const bool resc = need && (m != -INFINITY);
       float alpha = 1.f;
       if (need) {
-        alpha = resc ? fast_exp2(m_used - m_cand) : 0.f;
-        l *= alpha;
-        lr *= alpha;
-        m_used = m_cand;
+        alpha = resc ? fast_exp2(m - m_new) : 0.f;
+        const uint64_t a2 = f2_pack(alpha, alpha), z2 = f2_pack(0.f, 0.f);
+        l2 = f2_fma(l2, a2, z2);
+        lr2 = f2_fma(lr2, a2, z2);
+        m = m_new;
       }
+      // lazy rescale of O_t: PV_{j-1} has completed (it was issued before
+      // S_j, whose completion we just waited for); warp-collective accesses
       if (__any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
 #pragma unroll 1
@@ -349,42 +408,44 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           for (int i = 0; i < 32; ++i) ov[i] *= f;
           tmem_st32(tO + c * 32, ov);
         }
-        tmem_wait_st();
       }
-      // P_j (bf16) into shared memory, 128-byte swizzled, K-major
+      const float nm = (m == -INFINITY) ? 0.f : -m;
+      const uint64_t nm2 = f2_pack(nm, nm);
+      // P_j overwrites the first BK/2 columns of S_j (bf16 pairs), 32 at a time
 #pragma unroll
-      for (int u16 = 0; u16 < BK / 8; ++u16) {
-        float x[8];
+      for (int h = 0; h < BK / 64; ++h) {
+        uint32_t pw[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = u16 * 8 + i;
-          x[i] = (use && c < valid_cols) ? fast_exp2(fmaf(sv[c], p.scale_log2, -m_used)) : 0.f;
-          l += x[i];
+        for (int i = 0; i < 32; ++i) {
+          const int c = h * 64 + 2 * i;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(sv[c], sv[c + 1]), cl2, nm2), x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          const uint32_t w = pack_bf16(p0, p1);
+          pw[i] = w;
+          l2 = f2_add(l2, f2_pack(p0, p1));
+          lr2 = f2_add(lr2, f2_pack(bf16_lo(w), bf16_hi(w)));
         }
-        uint4 w;
-        w.x = pack_bf16(x[0], x[1]);
-        w.y = pack_bf16(x[2], x[3]);
-        w.z = pack_bf16(x[4], x[5]);
-        w.w = pack_bf16(x[6], x[7]);
-        lr += bf16_lo(w.x) + bf16_hi(w.x) + bf16_lo(w.y) + bf16_hi(w.y) + bf16_lo(w.z) +
-             bf16_hi(w.z) + bf16_lo(w.w) + bf16_hi(w.w);
-        const int chunk = u16 / 8, u = u16 % 8;
-        *reinterpret_cast<uint4 *>(sP + chunk * kTileM * 128 + r * 128 + ((u ^ (r & 7)) << 4)) = w;
+        tmem_st32u(tS + h * 32, pw);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[t]);
     }
-    if (ok && n_iter > 0) {
-      ok = mbar_wait(o_done, (n_iter - 1) & 1, kSiteODone, abort_flag);
+    if (ok && n > 0) {
+      ok = mbar_wait(&o_done[t], 0, kSiteODone, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok && n > 0) {
       tc_fence_after();
-      const int64_t orig = row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted]
-                                                 : row_sorted)
-                                     : 0;
-      const float inv_l = (lr > 0.f) ? 1.f / lr : 0.f;
+      float la, lb, ra, rb;
+      f2_unpack(l2, la, lb);
+      f2_unpack(lr2, ra, rb);
+      const float l = la + lb, lr = ra + rb;
+      const int64_t orig =
+          row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted] : row_sorted)
+                    : 0;
+      const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
       uint4 *orow = reinterpret_cast<uint4 *>(p.o + (static_cast<int64_t>(bh) * p.L + orig) * D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -395,16 +456,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 w;
-            w.x = pack_bf16(ov[q4 * 8 + 0] * inv_l, ov[q4 * 8 + 1] * inv_l);
-            w.y = pack_bf16(ov[q4 * 8 + 2] * inv_l, ov[q4 * 8 + 3] * inv_l);
-            w.z = pack_bf16(ov[q4 * 8 + 4] * inv_l, ov[q4 * 8 + 5] * inv_l);
-            w.w = pack_bf16(ov[q4 * 8 + 6] * inv_l, ov[q4 * 8 + 7] * inv_l);
+            w.x = pack_bf16(ov[q4 * 8 + 0] * inv, ov[q4 * 8 + 1] * inv);
+            w.y = pack_bf16(ov[q4 * 8 + 2] * inv, ov[q4 * 8 + 3] * inv);
+            w.z = pack_bf16(ov[q4 * 8 + 4] * inv, ov[q4 * 8 + 5] * inv);
+            w.w = pack_bf16(ov[q4 * 8 + 6] * inv, ov[q4 * 8 + 7] * inv);
             orow[c * 4 + q4] = w;
           }
         }
       }
       if (row_valid)
-        p.lse[static_cast<int64_t>(bh) * p.L + orig] = (m_used + log2f(l)) * 0.69314718055994531f;
+        p.lse[static_cast<int64_t>(bh) * p.L + orig] = (m + log2f(l)) * 0.69314718055994531f;
     }
     tc_fence_before();
   }
@@ -457,7 +518,7 @@ size_t attn_workspace_bytes(int64_t bh, int L, int D, bool perm_q, bool perm_k) 
   return (perm_q ? t : 0) + (perm_k ? 2 * t : 0);
 }
 
-template <int D, int BK>
+template <int D, int BK, bool kDense>
 static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                const AttnParams &p, int64_t bh, cudaStream_t st) {
   using Lay = AttnLayout<D, BK>;
@@ -466,13 +527,13 @@ static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, con
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_attn<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_attn<D, BK, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay::kAlloc);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const dim3 grid((p.L + kTileM - 1) / kTileM, static_cast<unsigned>(bh));
-  k_attn<D, BK><<<grid, kAttnThreads, Lay::kAlloc, st>>>(mq, mk, mv, p);
+  const dim3 grid((p.n_tiles + kTiles - 1) / kTiles, static_cast<unsigned>(bh));
+  k_attn<D, BK, kDense><<<grid, kAttnThreads, Lay::kAlloc, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -526,7 +587,7 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   p.L = L;
   p.N = (L + BK - 1) / BK;
   p.kappa = dense ? p.N : a.kappa;
-  p.dense = dense ? 1 : 0;
+  p.n_tiles = (L + kTileM - 1) / kTileM;
   p.block_idx = a.block_idx;
   p.perm_q = a.perm_q;
   p.o = static_cast<__nv_bfloat16 *>(a.o);
@@ -534,10 +595,15 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   const float scale = (a.scale > 0.f) ? a.scale : 1.0f / sqrtf(static_cast<float>(D));
   p.scale_log2 = scale * 1.4426950408889634f;
 
-  if (D == 128 && BK == 128) return launch_attn<128, 128>(mq, mk, mv, p, bh, st);
-  if (D == 128 && BK == 64) return launch_attn<128, 64>(mq, mk, mv, p, bh, st);
-  if (D == 64 && BK == 128) return launch_attn<64, 128>(mq, mk, mv, p, bh, st);
-  if (D == 64 && BK == 64) return launch_attn<64, 64>(mq, mk, mv, p, bh, st);
+  if (dense) {
+    if (D == 128) return launch_attn<128, 128, true>(mq, mk, mv, p, bh, st);
+    if (D == 64) return launch_attn<64, 128, true>(mq, mk, mv, p, bh, st);
+  } else {
+    if (D == 128 && BK == 128) return launch_attn<128, 128, false>(mq, mk, mv, p, bh, st);
+    if (D == 128 && BK == 64) return launch_attn<128, 64, false>(mq, mk, mv, p, bh, st);
+    if (D == 64 && BK == 128) return launch_attn<64, 128, false>(mq, mk, mv, p, bh, st);
+    if (D == 64 && BK == 64) return launch_attn<64, 64, false>(mq, mk, mv, p, bh, st);
+  }
   return cudaErrorInvalidValue;
 }
 
