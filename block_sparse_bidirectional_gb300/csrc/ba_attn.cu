@@ -3,28 +3,33 @@
 // Block Approximate Sparse Attention"), with the masked softmax of SparseD
 // §3.1 Eq. 3-4, and the same kernel run dense (Eq. 1).
 //
-// One CTA owns a tile of 128 consecutive sorted query rows (one query block
-// when B = 128, two when B = 64) and walks the key blocks its rows selected
-// (for B = 64: the union of the two lists, each entry tagged with which of
-// the two query blocks selected it; rows of the other block see -inf).
+// A CTA owns two tiles of 128 consecutive sorted query rows.  A tile is one
+// query block when B = 128, two when B = 64 (then it walks the union of the
+// two lists, each entry tagged with which block selected it; rows of the
+// other block see -inf for that entry).
 //
-// Warp roles (256 threads):
-//   warp 0       TMA producer: Q tile once, then K_j and V_j tiles of every
-//                listed key block into a 2-stage shared-memory ring
-//                (128-byte swizzle, 64-column boxes, 3-D maps so the ragged
-//                last block reads zeros instead of the next head).
+// Warp roles (384 threads; setmaxnreg moves registers to the softmax warps):
+//   warp 0       TMA producer: both Q tiles once, then every K_j and V_j
+//                block the MMA thread will consume, in that order, into one
+//                ring of shared-memory slots (128-byte swizzle, 64-column
+//                boxes, 3-D maps so a ragged last block reads zeros instead
+//                of the next head).  Dense mode: both tiles walk the same
+//                blocks, so each load serves both.
 //   warp 1       tensor-memory allocation and the single MMA-issuing thread:
-//                  S_j = Q K_j^T   -> TMEM (two S buffers, ping-pong), and
-//                  O  += P_j V_j   -> TMEM, V read as an MN-major operand;
-//                S_{j+1} is issued before waiting for P_j so the tensor core
-//                works while the softmax runs.
-//   warps 4-7    softmax + epilogue: thread t owns row t of the tile
-//                (TMEM lane t).  Online softmax in the log2 domain with a
-//                lazy rescale: O in TMEM is corrected only when the running
-//                max grows by more than 2^8.  P (bf16) goes to shared memory
-//                in the swizzled K-major layout the MMA reads.  At the end
-//                O / l is written as bf16 to the ORIGINAL row pi_q(r), and
-//                LSE = ln(sum exp(scale q.k)).
+//                  S_t = Q_t K_j^T        -> TMEM (one S buffer per tile)
+//                  O_t += P_t V_j         -> TMEM, P_t read from TMEM as the A
+//                                            operand, V as an MN-major operand
+//                alternating tiles so the tensor core works on one tile
+//                while the other tile's softmax runs.  S_t(j+1) is issued
+//                right after PV_t(j) and overwrites P_t in place (tcgen05 MMAs
+//                of one thread execute in order).
+//   warps 4-7,   softmax + epilogue for tile 0 and tile 1: thread r owns row r
+//   warps 8-11   (TMEM lane r).  Online softmax in the log2 domain with a lazy
+//                rescale: O_t is corrected only when the running max grows by
+//                more than 2^8, and then without waiting (PV_t(j-1) completed
+//                before S_t(j) did).  P (bf16 pairs) is stored over S_t.  At
+//                the end O / l is written as bf16 to the ORIGINAL row pi_q(r),
+//                and LSE = ln(sum exp(scale q.k)).
 // Every wait is bounded; on a timeout the CTA records the site in the device
 // error word, drains its in-flight copies / MMAs and frees tensor memory.
 #include <cuda.h>
@@ -56,9 +61,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 constexpr int next_pow2_cols(int x) {
   int c = 32;
@@ -359,12 +361,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const float cl = p.scale_log2;
     const uint64_t cl2 = f2_pack(cl, cl);
     float m = -INFINITY;
-    uint64_t l2 = f2_pack(0.f, 0.f);   // exact weights: for the LSE
-    uint64_t lr2 = f2_pack(0.f, 0.f);  // bf16-rounded weights: normalise O
+    uint64_t l2 = f2_pack(0.f, 0.f);  // running sum of the fp32 weights (two halves)
     bool ok = true;
     const int n = n_t[t];
+    int my_blk = 0;  // sparse, one query block per tile: 32 list entries, one per lane
     for (int j = 0; j < n; ++j) {
-      const uint32_t e = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j);
+      uint32_t e;
+      if (!kDense && G == 1) {
+        if ((j & 31) == 0)
+          my_blk = (j + lane < n) ? min(max(__ldg(idx_t[t] + j + lane), 0), p.N - 1) : 0;
+        e = static_cast<uint32_t>(__shfl_sync(0xffffffffu, my_blk, j & 31)) | (1u << 12);
+      } else {
+        e = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j);
+      }
       const int blk = e & 0xFFF;
       const bool sel = (e >> (12 + my_g)) & 1u;
       const int valid_cols = min(BK, p.L - blk * BK);
@@ -392,7 +401,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         alpha = resc ? fast_exp2(m - m_new) : 0.f;
         const uint64_t a2 = f2_pack(alpha, alpha), z2 = f2_pack(0.f, 0.f);
         l2 = f2_fma(l2, a2, z2);
-        lr2 = f2_fma(lr2, a2, z2);
         m = m_new;
       }
       // lazy rescale of O_t: PV_{j-1} has completed (it was issued before
@@ -424,7 +432,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           const uint32_t w = pack_bf16(p0, p1);
           pw[i] = w;
           l2 = f2_add(l2, f2_pack(p0, p1));
-          lr2 = f2_add(lr2, f2_pack(bf16_lo(w), bf16_hi(w)));
         }
         tmem_st32u(tS + h * 32, pw);
       }
@@ -438,14 +445,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     if (ok && n > 0) {
       tc_fence_after();
-      float la, lb, ra, rb;
+      float la, lb;
       f2_unpack(l2, la, lb);
-      f2_unpack(lr2, ra, rb);
-      const float l = la + lb, lr = ra + rb;
+      const float l = la + lb;
       const int64_t orig =
           row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted] : row_sorted)
                     : 0;
-      const float inv = (lr > 0.f) ? 1.f / lr : 0.f;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
       uint4 *orow = reinterpret_cast<uint4 *>(p.o + (static_cast<int64_t>(bh) * p.L + orig) * D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
