@@ -5,21 +5,25 @@
 //   k_sqnorm_keys   Eq. 9: fp32 squared norm of every Q / K row, packed with
 //                   the token index into a 64-bit sort key.  One streaming
 //                   pass over Q and K (16-byte vector loads, coalesced).
-//   k_chunk_sort    Eq. 10: bitonic sort of 4096-key chunks in shared memory.
+//   k_chunk_sort    Eq. 10: 4096-key chunks: each warp sorts 256 keys in
+//                   registers (bitonic network, shuffles), the CTA merges the
+//                   runs in shared memory.
 //   k_merge_pass    merge-path merge of sorted runs (width doubles per pass);
 //                   the last pass emits pi (sorted position -> token index).
 //                   Keys are unique (index in the low word), so the result is
 //                   the stable sort.
-//   k_block_stats   Algorithm 1 step 4: gathers the rows of one sorted block
-//                   through pi into shared memory; fp32 mean and population
-//                   variance per feature; writes the augmented vectors
+//   k_block_stats   Algorithm 1 step 4: gathers the rows of sorted blocks
+//                   through pi into shared memory (cp.async, double-buffered
+//                   across the blocks a CTA walks); two-pass fp32 mean and
+//                   population variance per feature; writes
 //                     a = [Qbar/sqrt(d), beta/d*VarQ, beta/d*Qbar^2]
 //                     b = [Kbar, Kbar^2 + VarK, VarK]
 //                   so that a.b = Eq. 2 + beta * Eq. 14 (Eq. 13).
 //   k_scores        l'[gq,gk] = a_gq . b_gk: a batched fp32 SIMT GEMM
-//                   (64x64 tiles, 4x4 register micro-tiles).  Kept on the
+//                   (128x128 tiles, 8x8 register micro-tiles, f32x2 FMAs).  Kept on the
 //                   fp32 ALUs so the top-kappa decision is taken in fp32.
-//   k_topk          steps 8-11: one warp per query-block row; MSB-first radix
+//   k_topk          steps 8-11: one warp per query-block row, keys held in
+//                   registers; MSB-first radix
 //                   select of the kappa-th largest score on order-preserving
 //                   integer keys (warp reductions), ties to the lower block
 //                   index; emits the ascending index list and the bitmask.
@@ -34,50 +38,66 @@
 
 namespace ba {
 
-constexpr int kChunk = 4096;          // keys sorted per CTA in shared memory
-constexpr int kChunkThreads = 1024;
+constexpr int kChunk = 4096;          // keys sorted per CTA (16 warps x 256)
+constexpr int kSortThreads = 512;
 constexpr int kMergeThreads = 256;
 constexpr int kMergeItems = 8;        // outputs per merge thread
 constexpr int kStatsThreads = 256;
 constexpr int kTopkWarps = 4;
+constexpr int kNormRowsPerThread = 4;
 
 // ---------------------------------------------------------------------------
-// step 1-2a: squared norms -> sort keys
+// step 1-2a: squared norms -> sort keys.  grid = (.., sorted tensors)
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__restrict__ x,
+__global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__restrict__ x0,
+                                                     const __nv_bfloat16 *__restrict__ x1,
                                                      uint64_t *__restrict__ keys, int64_t rows,
                                                      int L) {
-  constexpr int TPR = D / 8;  // threads per row, 8 bf16 (16 B) each
-  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = gtid / TPR;
-  const int part = static_cast<int>(gtid % TPR);
-  float acc = 0.f;
-  if (row < rows) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + row * D) + part);
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+  constexpr int TPR = D / 8;            // threads per row, 8 bf16 (16 B) each
+  constexpr int RPW = 256 / TPR;        // rows per 256-thread wave
+  const __nv_bfloat16 *x = blockIdx.y == 0 ? x0 : x1;
+  uint64_t *out = keys + static_cast<int64_t>(blockIdx.y) * rows;
+  const int part = threadIdx.x % TPR;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPW * kNormRowsPerThread + threadIdx.x / TPR;
+  uint4 raw[kNormRowsPerThread];
+#pragma unroll
+  for (int u = 0; u < kNormRowsPerThread; ++u) {
+    const int64_t row = row0 + u * RPW;
+    raw[u] = (row < rows) ? __ldg(reinterpret_cast<const uint4 *>(x + row * D) + part)
+                          : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int u = 0; u < kNormRowsPerThread; ++u) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw[u]);
+    float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float2 f = __bfloat1622float2(h[i]);
       acc = fmaf(f.x, f.x, acc);
       acc = fmaf(f.y, f.y, acc);
     }
-  }
 #pragma unroll
-  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < rows && part == 0) {
-    const uint32_t tok = static_cast<uint32_t>(row % L);
-    keys[row] = (static_cast<uint64_t>(__float_as_uint(acc)) << 32) | tok;
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    const int64_t row = row0 + u * RPW;
+    if (row < rows && part == 0) {
+      const uint32_t tok = static_cast<uint32_t>(row % L);
+      out[row] = (static_cast<uint64_t>(__float_as_uint(acc)) << 32) | tok;
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
-// step 1-2b: chunk sort.  grid = (chunks per window, windows, sequences)
+// step 1-2b: chunk sort.  grid = (chunks per window, windows, sorted sequences)
+// A warp sorts 256 keys in registers (bitonic network, 8 keys per lane,
+// shuffles across lanes); the CTA then merges the 16 runs in shared memory
+// (merge path, 4 levels).  Keys are unique, so the order is the stable one.
 // ---------------------------------------------------------------------------
 struct SortGeom {
   int L;        // tokens per sequence
   int win;      // window length (== L for a whole-sequence sort)
   int nwin;     // windows per sequence
+  int bh;       // sequences per tensor
 };
 
 __device__ __forceinline__ int window_len(const SortGeom &g, int w) {
@@ -85,67 +105,8 @@ __device__ __forceinline__ int window_len(const SortGeom &g, int w) {
   return min(g.win, g.L - start);
 }
 
-__global__ void __launch_bounds__(kChunkThreads) k_chunk_sort(const uint64_t *__restrict__ keys_in,
-                                                              uint64_t *__restrict__ keys_out,
-                                                              int32_t *__restrict__ perm_out,
-                                                              SortGeom g, int final_pass) {
-  __shared__ uint64_t s[kChunk];
-  const int w = blockIdx.y;
-  const int seq = blockIdx.z;
-  const int wlen = window_len(g, w);
-  const int c0 = blockIdx.x * kChunk;
-  if (c0 >= wlen) return;  // uniform over the CTA
-  const int n = min(kChunk, wlen - c0);
-  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win + c0;
-  for (int i = threadIdx.x; i < kChunk; i += kChunkThreads)
-    s[i] = (i < n) ? keys_in[base + i] : ~0ull;
-  __syncthreads();
-  for (int k = 2; k <= kChunk; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int p = threadIdx.x; p < kChunk / 2; p += kChunkThreads) {
-        const int i = 2 * j * (p / j) + (p % j);
-        const int q = i + j;
-        const bool up = (i & k) == 0;
-        const uint64_t a = s[i], b = s[q];
-        if ((a > b) == up) {
-          s[i] = b;
-          s[q] = a;
-        }
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < n; i += kChunkThreads) {
-    if (final_pass)
-      perm_out[base + i] = static_cast<int32_t>(s[i] & 0xffffffffu);
-    else
-      keys_out[base + i] = s[i];
-  }
-}
-
-// ---------------------------------------------------------------------------
-// step 1-2c: merge pass.  Runs of `width` inside each window are merged in
-// pairs.  grid = (ceil(win / (threads*items)), windows, sequences)
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__restrict__ in,
-                                                              uint64_t *__restrict__ out,
-                                                              int32_t *__restrict__ perm_out,
-                                                              SortGeom g, int width,
-                                                              int final_pass) {
-  const int w = blockIdx.y;
-  const int seq = blockIdx.z;
-  const int wlen = window_len(g, w);
-  const int o0 = (blockIdx.x * kMergeThreads + threadIdx.x) * kMergeItems;
-  if (o0 >= wlen) return;
-  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win;
-  const int pair = o0 / (2 * width);
-  const int p0 = pair * 2 * width;
-  const int a0 = p0, a1 = min(p0 + width, wlen);
-  const int b0 = a1, b1 = min(p0 + 2 * width, wlen);
-  const int la = a1 - a0, lb = b1 - b0;
-  const uint64_t *A = in + base + a0;
-  const uint64_t *B = in + base + b0;
-  const int diag = o0 - p0;
+__device__ __forceinline__ void merge_path_8(const uint64_t *A, const uint64_t *B, int la, int lb,
+                                             int diag, int n, uint64_t *dst) {
   int lo = max(0, diag - lb), hi = min(diag, la);
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
@@ -155,18 +116,189 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
       hi = mid;
   }
   int i = lo, j = diag - lo;
-  const int n = min(kMergeItems, (la + lb) - diag);
   for (int t = 0; t < n; ++t) {
-    uint64_t v;
     if (i < la && (j >= lb || A[i] < B[j]))
-      v = A[i++];
+      dst[t] = A[i++];
     else
-      v = B[j++];
-    const int64_t dst = base + o0 + t;
+      dst[t] = B[j++];
+  }
+}
+
+// Shared-memory arrays of 64-bit keys are padded with one word per 8 so that
+// threads walking runs that start 8 keys apart hit distinct banks.
+__device__ __forceinline__ int spad(int i) { return i + (i >> 3); }
+constexpr int spad_size(int n) { return n + (n >> 3); }
+
+// merge_path_8 over padded shared-memory runs: A = s[a0 ..), B = s[b0 ..)
+__device__ __forceinline__ void merge_path_8_smem(const uint64_t *s, int a0, int b0, int la,
+                                                  int lb, int diag, int n, uint64_t *dst,
+                                                  int d0) {
+  int lo = max(0, diag - lb), hi = min(diag, la);
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s[spad(a0 + mid)] < s[spad(b0 + diag - 1 - mid)])
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  int i = lo, j = diag - lo;
+  uint64_t va = (i < la) ? s[spad(a0 + i)] : ~0ull;
+  uint64_t vb = (j < lb) ? s[spad(b0 + j)] : ~0ull;
+  for (int t = 0; t < n; ++t) {
+    const bool take_a = (i < la) && (j >= lb || va < vb);
+    if (take_a) {
+      dst[spad(d0 + t)] = va;
+      ++i;
+      va = (i < la) ? s[spad(a0 + i)] : ~0ull;
+    } else {
+      dst[spad(d0 + t)] = vb;
+      ++j;
+      vb = (j < lb) ? s[spad(b0 + j)] : ~0ull;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__restrict__ keys_in,
+                                                             uint64_t *__restrict__ keys_out,
+                                                             int32_t *__restrict__ perm0,
+                                                             int32_t *__restrict__ perm1,
+                                                             SortGeom g, int final_pass) {
+  extern __shared__ __align__(16) uint64_t sbuf[];  // 2 x padded kChunk
+  uint64_t *sa = sbuf, *sb = sbuf + spad_size(kChunk);
+  const int w = blockIdx.y;
+  const int seq = blockIdx.z;
+  const int wlen = window_len(g, w);
+  const int c0 = blockIdx.x * kChunk;
+  if (c0 >= wlen) return;  // uniform over the CTA
+  const int n = min(kChunk, wlen - c0);
+  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win + c0;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // ---- warp-level bitonic sort of 256 keys; element e = i * 32 + lane ----
+  // (striped, so the loads coalesce).  Partner e ^ j: lane ^ j for j < 32,
+  // register i ^ (j / 32) for j >= 32.
+  uint64_t r[8];
+  const int w0 = warp * 256;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = w0 + i * 32 + lane;
+    r[i] = (e < n) ? keys_in[base + e] : ~0ull;
+  }
+#pragma unroll
+  for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j < 32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int e = i * 32 + lane;
+          const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
+          const uint64_t y = __shfl_xor_sync(0xffffffffu, r[i], j);
+          r[i] = keep_min ? (r[i] < y ? r[i] : y) : (r[i] < y ? y : r[i]);
+        }
+      } else {
+        const int ij = j >> 5;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i & ij) continue;
+          const int i2 = i | ij;
+          const bool up = (((i * 32 + lane) & k) == 0);
+          const uint64_t a = r[i], b = r[i2];
+          if ((a > b) == up) {
+            r[i] = b;
+            r[i2] = a;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sa[spad(w0 + i * 32 + lane)] = r[i];
+  __syncthreads();
+
+  // ---- merge the 16 sorted runs: 256 -> 512 -> 1024 -> 2048 -> 4096 ----
+  uint64_t *src = sa, *dst = sb;
+  for (int width = 256; width < kChunk; width <<= 1) {
+    const int o0 = threadIdx.x * 8;
+    const int p0 = (o0 / (2 * width)) * 2 * width;
+    merge_path_8_smem(src, p0, p0 + width, width, width, o0 - p0, 8, dst, o0);
+    __syncthreads();
+    uint64_t *t = src;
+    src = dst;
+    dst = t;
+  }
+  int32_t *perm = (seq < g.bh) ? perm0 : perm1;
+  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + static_cast<int64_t>(w) * g.win + c0;
+  for (int i = threadIdx.x; i < n; i += kSortThreads) {
     if (final_pass)
-      perm_out[dst] = static_cast<int32_t>(v & 0xffffffffu);
+      perm[pbase + i] = static_cast<int32_t>(src[spad(i)] & 0xffffffffu);
     else
-      out[dst] = v;
+      keys_out[base + i] = src[spad(i)];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// step 1-2c: merge pass.  Runs of `width` inside each window are merged in
+// pairs.  grid = (ceil(win / (threads*items)), windows, sorted sequences)
+// ---------------------------------------------------------------------------
+// Each CTA produces kMergeTile consecutive outputs of one merged pair: one
+// merge-path split per CTA boundary, the two input ranges staged in shared
+// memory with coalesced loads, per-thread merges of kMergeItems from shared
+// memory, coalesced stores.
+constexpr int kMergeTile = kMergeThreads * kMergeItems;
+
+__global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__restrict__ in,
+                                                              uint64_t *__restrict__ out,
+                                                              int32_t *__restrict__ perm0,
+                                                              int32_t *__restrict__ perm1,
+                                                              SortGeom g, int width,
+                                                              int final_pass) {
+  __shared__ uint64_t s_in[spad_size(kMergeTile)];
+  __shared__ uint64_t s_out[spad_size(kMergeTile)];
+  __shared__ int s_split[2];
+  const int w = blockIdx.y;
+  const int seq = blockIdx.z;
+  const int wlen = window_len(g, w);
+  const int o_cta = blockIdx.x * kMergeTile;
+  if (o_cta >= wlen) return;  // uniform over the CTA
+  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win;
+  const int p0 = (o_cta / (2 * width)) * 2 * width;
+  const int a1 = min(p0 + width, wlen), b1 = min(p0 + 2 * width, wlen);
+  const int la = a1 - p0, lb = b1 - a1;
+  const uint64_t *A = in + base + p0;
+  const uint64_t *B = in + base + a1;
+  const int d0 = o_cta - p0;
+  const int cnt = min(kMergeTile, la + lb - d0);
+  if (threadIdx.x < 2) {
+    const int diag = d0 + (threadIdx.x == 0 ? 0 : cnt);
+    int lo = max(0, diag - lb), hi = min(diag, la);
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (A[mid] < B[diag - 1 - mid])
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    s_split[threadIdx.x] = lo;
+  }
+  __syncthreads();
+  const int ia0 = s_split[0], ia1 = s_split[1];
+  const int ib0 = d0 - ia0, ib1 = d0 + cnt - ia1;
+  const int na = ia1 - ia0, nb = ib1 - ib0;  // na + nb == cnt
+  for (int i = threadIdx.x; i < na; i += kMergeThreads) s_in[spad(i)] = A[ia0 + i];
+  for (int i = threadIdx.x; i < nb; i += kMergeThreads) s_in[spad(na + i)] = B[ib0 + i];
+  __syncthreads();
+  const int t0 = threadIdx.x * kMergeItems;
+  if (t0 < cnt)
+    merge_path_8_smem(s_in, 0, na, na, nb, t0, min(kMergeItems, cnt - t0), s_out, t0);
+  __syncthreads();
+  int32_t *perm = (seq < g.bh) ? perm0 : perm1;
+  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + static_cast<int64_t>(w) * g.win;
+  for (int i = threadIdx.x; i < cnt; i += kMergeThreads) {
+    if (final_pass)
+      perm[pbase + o_cta + i] = static_cast<int32_t>(s_out[spad(i)] & 0xffffffffu);
+    else
+      out[base + o_cta + i] = s_out[spad(i)];
   }
 }
 
@@ -176,123 +308,185 @@ __global__ void k_iota(int32_t *__restrict__ perm, int64_t total, int L) {
 }
 
 // ---------------------------------------------------------------------------
-// step 3-4: block statistics -> augmented vectors.  grid = (N, b*h)
+// step 3-4: block statistics -> augmented vectors.
+// grid = (ceil(N / kStatsBlocksPerCta), b*h, 2): z = 0 for Q (query side),
+// 1 for K.  A CTA walks kStatsBlocksPerCta consecutive sorted blocks; the
+// rows of the next block are gathered through pi into a second shared-memory
+// stage with cp.async while the current block is reduced (two passes: mean,
+// then mean squared deviation, one feature per thread and row slice).
 // ---------------------------------------------------------------------------
-template <int D>
+constexpr int kStatsBlocksPerCta = 4;
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int D, int BK>
 __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
-    const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ perm, int L, int B, int N,
-    float *__restrict__ aug, int query_side, float beta) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  __nv_bfloat16 *rows = reinterpret_cast<__nv_bfloat16 *>(smem_raw);          // [B][D]
-  float *red = reinterpret_cast<float *>(smem_raw + static_cast<size_t>(B) * D * 2);  // [P][D]
+    const __nv_bfloat16 *__restrict__ xq, const __nv_bfloat16 *__restrict__ xk,
+    const int32_t *__restrict__ perm_q, const int32_t *__restrict__ perm_k, int L, int N,
+    float *__restrict__ aug_q, float *__restrict__ aug_k, float beta) {
+  constexpr int VPR = D / 8;             // 16-byte vectors per row
+  constexpr int P = kStatsThreads / D;   // row slices per feature
+  extern __shared__ __align__(16) unsigned char st_raw[];
+  __nv_bfloat16 *stage[2] = {reinterpret_cast<__nv_bfloat16 *>(st_raw),
+                             reinterpret_cast<__nv_bfloat16 *>(st_raw) + BK * D};
+  int *s_src = reinterpret_cast<int *>(st_raw + 2 * BK * D * 2);  // [bpc][BK]
+  __shared__ float red[P][D];
   __shared__ float s_mean[D];
-
-  constexpr int P = kStatsThreads / D;
-  const int g = blockIdx.x;
+  const bool qside = blockIdx.z == 0;
+  const __nv_bfloat16 *x = qside ? xq : xk;
+  const int32_t *perm = qside ? perm_q : perm_k;
+  float *aug = qside ? aug_q : aug_k;
   const int64_t bh = blockIdx.y;
-  const int r0 = g * B;
-  const int n = min(B, L - r0);
+  const int g0 = blockIdx.x * kStatsBlocksPerCta;
+  const int nblk = min(kStatsBlocksPerCta, N - g0);
   const __nv_bfloat16 *xs = x + bh * static_cast<int64_t>(L) * D;
-  const int32_t *ps = perm + bh * static_cast<int64_t>(L) + r0;
 
-  constexpr int VPR = D / 8;  // 16-byte vectors per row
-  for (int idx = threadIdx.x; idx < n * VPR; idx += kStatsThreads) {
-    const int r = idx / VPR, c = idx % VPR;
-    const int src = __ldg(ps + r);
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xs + static_cast<int64_t>(src) * D) + c);
-    reinterpret_cast<uint4 *>(rows + r * D)[c] = v;
+  // source rows of every block this CTA reduces
+  for (int i = threadIdx.x; i < nblk * BK; i += kStatsThreads) {
+    const int r = g0 * BK + i;
+    s_src[i] = (r < L) ? __ldg(perm + bh * static_cast<int64_t>(L) + r) : -1;
   }
   __syncthreads();
-
-  const int dim = threadIdx.x % D;
-  const int part = threadIdx.x / D;
-  float acc = 0.f;
-  for (int r = part; r < n; r += P) acc += __bfloat162float(rows[r * D + dim]);
-  red[part * D + dim] = acc;
-  __syncthreads();
-  if (threadIdx.x < D) {
-    float s = 0.f;
-#pragma unroll
-    for (int p = 0; p < P; ++p) s += red[p * D + dim];
-    s_mean[dim] = s / static_cast<float>(n);
-  }
-  __syncthreads();
-  const float mean = s_mean[dim];
-  acc = 0.f;
-  for (int r = part; r < n; r += P) {
-    const float dv = __bfloat162float(rows[r * D + dim]) - mean;
-    acc = fmaf(dv, dv, acc);
-  }
-  __syncthreads();
-  red[part * D + dim] = acc;
-  __syncthreads();
-  if (threadIdx.x < D) {
-    float s = 0.f;
-#pragma unroll
-    for (int p = 0; p < P; ++p) s += red[p * D + dim];
-    const float var = s / static_cast<float>(n);
-    float *o = aug + (bh * N + g) * static_cast<int64_t>(3 * D);
-    if (query_side) {
-      const float c = beta / static_cast<float>(D);
-      o[dim] = mean * rsqrtf(static_cast<float>(D));
-      o[D + dim] = c * var;
-      o[2 * D + dim] = c * mean * mean;
-    } else {
-      o[dim] = mean;
-      o[D + dim] = fmaf(mean, mean, var);
-      o[2 * D + dim] = var;
+  auto issue = [&](int bi) {
+    __nv_bfloat16 *dst = stage[bi & 1];
+    for (int idx = threadIdx.x; idx < BK * VPR; idx += kStatsThreads) {
+      const int r = idx / VPR, c = idx % VPR;
+      const int src = s_src[bi * BK + r];
+      if (src >= 0) cp_async16(dst + r * D + c * 8, xs + static_cast<int64_t>(src) * D + c * 8);
     }
+    cp_async_commit();
+  };
+  issue(0);
+  const int dim = threadIdx.x % D, part = threadIdx.x / D;
+  for (int bi = 0; bi < nblk; ++bi) {
+    if (bi + 1 < nblk) {
+      issue(bi + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const __nv_bfloat16 *rows = stage[bi & 1];
+    const int g = g0 + bi;
+    const int n = min(BK, L - g * BK);
+    float acc = 0.f;
+    for (int r = part; r < n; r += P) acc += __bfloat162float(rows[r * D + dim]);
+    red[part][dim] = acc;
+    __syncthreads();
+    if (threadIdx.x < D) {
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < P; ++q) sum += red[q][dim];
+      s_mean[dim] = sum / static_cast<float>(n);
+    }
+    __syncthreads();
+    const float mean = s_mean[dim];
+    acc = 0.f;
+    for (int r = part; r < n; r += P) {
+      const float dv = __bfloat162float(rows[r * D + dim]) - mean;
+      acc = fmaf(dv, dv, acc);
+    }
+    red[part][dim] = acc;
+    __syncthreads();
+    if (threadIdx.x < D) {
+      float sum = 0.f;
+#pragma unroll
+      for (int q = 0; q < P; ++q) sum += red[q][dim];
+      const float var = sum / static_cast<float>(n);
+      float *o = aug + (bh * N + g) * static_cast<int64_t>(3 * D);
+      if (qside) {
+        const float cf = beta / static_cast<float>(D);
+        o[dim] = mean * rsqrtf(static_cast<float>(D));
+        o[D + dim] = cf * var;
+        o[2 * D + dim] = cf * mean * mean;
+      } else {
+        o[dim] = mean;
+        o[D + dim] = fmaf(mean, mean, var);
+        o[2 * D + dim] = var;
+      }
+    }
+    __syncthreads();  // the stage is refilled two iterations on
   }
 }
 
 // ---------------------------------------------------------------------------
 // step 5-7: scores = A . B^T per (b,h); A, B are [N][KS] rows with stride 3D.
-// grid = (ceil(N/64), ceil(N/64), b*h)
+// grid = (ceil(N/128), ceil(N/128), b*h); 128x128 tiles, 8x8 register
+// micro-tiles, packed f32x2 FMAs.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
                                                 const float *__restrict__ Bm,
                                                 float *__restrict__ C, int N, int KS,
                                                 int stride) {
-  constexpr int BM = 64, BK = 16, PAD = 4;
-  __shared__ __align__(16) float As[BK][BM + PAD];
-  __shared__ __align__(16) float Bs[BK][BM + PAD];
+  constexpr int BM = 128, BKK = 8, PAD = 4;
+  __shared__ __align__(16) float As[BKK][BM + PAD];
+  __shared__ __align__(16) float Bs[BKK][BM + PAD];
   const int64_t bh = blockIdx.z;
   const float *Ab = A + bh * N * static_cast<int64_t>(stride);
   const float *Bb = Bm + bh * N * static_cast<int64_t>(stride);
   const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BM;
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;
-  const int lr = tid / 4, lk = (tid % 4) * 4;  // loader: row, k offset
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < KS; k0 += BK) {
-    float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
-    if (i0 + lr < N) va = *reinterpret_cast<const float4 *>(Ab + (i0 + lr) * static_cast<int64_t>(stride) + k0 + lk);
-    if (j0 + lr < N) vb = *reinterpret_cast<const float4 *>(Bb + (j0 + lr) * static_cast<int64_t>(stride) + k0 + lk);
+  const int lr = tid / 2, lk = (tid % 2) * 4;  // loader: row, k offset
+  uint64_t acc[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0ull;
+  const float *arow = Ab + (i0 + lr) * static_cast<int64_t>(stride) + lk;
+  const float *brow = Bb + (j0 + lr) * static_cast<int64_t>(stride) + lk;
+  const bool a_ok = i0 + lr < N, b_ok = j0 + lr < N;
+  float4 na4 = a_ok ? *reinterpret_cast<const float4 *>(arow) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < KS; k0 += BKK) {
+    const float4 va = na4, vb = nb4;
+    if (k0 + BKK < KS) {  // prefetch the next chunk while this one is used
+      na4 = a_ok ? *reinterpret_cast<const float4 *>(arow + k0 + BKK) : make_float4(0.f, 0.f, 0.f, 0.f);
+      nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow + k0 + BKK) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     As[lk + 0][lr] = va.x; As[lk + 1][lr] = va.y; As[lk + 2][lr] = va.z; As[lk + 3][lr] = va.w;
     Bs[lk + 0][lr] = vb.x; Bs[lk + 1][lr] = vb.y; Bs[lk + 2][lr] = vb.z; Bs[lk + 3][lr] = vb.w;
     __syncthreads();
 #pragma unroll
-    for (int kk = 0; kk < BK; ++kk) {
-      const float4 a = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
-      const float4 b = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
-      const float av[4] = {a.x, a.y, a.z, a.w};
-      const float bv[4] = {b.x, b.y, b.z, b.w};
+    for (int kk = 0; kk < BKK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 8 + 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint64_t bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
+                              f2_pack(b1.z, b1.w)};
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 8; ++r) {
+        const uint64_t a2 = f2_pack(av[r], av[r]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+        for (int c = 0; c < 4; ++c) acc[r][c] = f2_fma(a2, bp[c], acc[r][c]);
+      }
     }
     __syncthreads();
   }
   float *Cb = C + bh * N * static_cast<int64_t>(N);
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = i0 + ty * 4 + r;
+  for (int r = 0; r < 8; ++r) {
+    const int i = i0 + ty * 8 + r;
     if (i >= N) continue;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int j = j0 + tx * 4 + c;
-      if (j < N) Cb[i * static_cast<int64_t>(N) + j] = acc[r][c];
+      float x0, x1;
+      f2_unpack(acc[r][c], x0, x1);
+      const int j = j0 + tx * 8 + 2 * c;
+      if (j < N) Cb[i * static_cast<int64_t>(N) + j] = x0;
+      if (j + 1 < N) Cb[i * static_cast<int64_t>(N) + j + 1] = x1;
     }
   }
 }
@@ -306,37 +500,45 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Keys of one row live in registers (KPL per lane, element e = i * 32 + lane).
+template <int KPL>
 __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(const float *__restrict__ scores,
                                                           int64_t rows, int N, int kappa,
                                                           int32_t *__restrict__ idx,
                                                           uint32_t *__restrict__ mask) {
-  extern __shared__ uint32_t skeys[];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kTopkWarps + warp;
   if (row >= rows) return;  // warp-uniform; no block barrier below
-  uint32_t *keys = skeys + warp * N;
   const float *src = scores + row * N;
-  for (int e = lane; e < N; e += 32) keys[e] = order_key(src[e]);
-  __syncwarp();
+  uint32_t keys[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = i * 32 + lane;
+    keys[i] = (e < N) ? order_key(src[e]) : 0u;  // 0 sorts below every real key
+  }
   uint32_t T = 0;
   for (int bit = 31; bit >= 0; --bit) {
     const uint32_t cand = T | (1u << bit);
     uint32_t cnt = 0;
-    for (int e = lane; e < N; e += 32) cnt += keys[e] >= cand;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) cnt += (i * 32 + lane < N) && keys[i] >= cand;
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (cnt >= static_cast<uint32_t>(kappa)) T = cand;
   }
   uint32_t gt = 0;
-  for (int e = lane; e < N; e += 32) gt += keys[e] > T;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) gt += (i * 32 + lane < N) && keys[i] > T;
   gt = __reduce_add_sync(0xffffffffu, gt);
   const int need = kappa - static_cast<int>(gt);  // >= 1 equal keys to take
   const int nwords = (N + 31) / 32;
   const uint32_t lt_mask = (1u << lane) - 1u;
   int taken = 0, base = 0;
-  for (int wd = 0; wd < nwords; ++wd) {
+#pragma unroll
+  for (int wd = 0; wd < KPL; ++wd) {
+    if (wd >= nwords) break;
     const int e = wd * 32 + lane;
     const bool valid = e < N;
-    const uint32_t key = valid ? keys[e] : 0u;
+    const uint32_t key = keys[wd];
     const uint32_t eqb = __ballot_sync(0xffffffffu, valid && key == T);
     const int rem = need - taken;
     const bool sel_eq = valid && key == T && __popc(eqb & lt_mask) < rem;
@@ -377,30 +579,43 @@ size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode) {
   return plan_select(bh, L, D, B, sort_mode, true).total;
 }
 
+// Sorts `nseq` sequences of L keys (windows of `win`), writing pi into
+// perm0 (the first `bh` sequences) and perm1 (the rest).
 static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t *buf1,
-                                  int32_t *perm, int nseq, int L, int win, cudaStream_t st) {
+                                  int32_t *perm0, int32_t *perm1, int nseq, int64_t bh, int L,
+                                  int win, cudaStream_t st) {
   SortGeom g;
   g.L = L;
   g.win = (win <= 0 || win >= L) ? L : win;
   g.nwin = (L + g.win - 1) / g.win;
+  g.bh = static_cast<int>(bh);
   int npasses = 0;
   for (int w = kChunk; w < g.win; w <<= 1) ++npasses;
   const int chunks = (g.win + kChunk - 1) / kChunk;
-  // chunk sort: keys -> buf0 (or perm when no merge pass follows)
-  k_chunk_sort<<<dim3(chunks, g.nwin, nseq), kChunkThreads, 0, st>>>(keys, buf0, perm, g,
-                                                                     npasses == 0);
-  cudaError_t e = cudaGetLastError();
+  const size_t smem = 2 * spad_size(kChunk) * sizeof(uint64_t);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(k_chunk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  // chunk sort: keys -> buf0 (or pi when no merge pass follows)
+  k_chunk_sort<<<dim3(chunks, g.nwin, nseq), kSortThreads, smem, st>>>(keys, buf0, perm0, perm1,
+                                                                        g, npasses == 0);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const uint64_t *src = buf0;
   uint64_t *dst = buf1;
   int width = kChunk;
   for (int p = 0; p < npasses; ++p) {
     const int per_cta = kMergeThreads * kMergeItems;
     const int gx = (g.win + per_cta - 1) / per_cta;
-    k_merge_pass<<<dim3(gx, g.nwin, nseq), kMergeThreads, 0, st>>>(src, dst, perm, g, width,
-                                                                   p == npasses - 1);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    k_merge_pass<<<dim3(gx, g.nwin, nseq), kMergeThreads, 0, st>>>(src, dst, perm0, perm1, g,
+                                                                   width, p == npasses - 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const uint64_t *t = dst;
     dst = const_cast<uint64_t *>(src);
     src = t;
@@ -409,14 +624,24 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
   return cudaSuccess;
 }
 
-template <int D>
-static cudaError_t launch_stats(const void *x, const int32_t *perm, int64_t bh, int L, int B,
-                                int N, float *aug, int query_side, float beta, cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(B) * D * 2 + (kStatsThreads / D) * D * sizeof(float);
-  static bool attr_set = false;  // smem <= 40 KB, below the default 48 KB limit
-  (void)attr_set;
-  k_block_stats<D><<<dim3(N, static_cast<unsigned>(bh)), kStatsThreads, smem, st>>>(
-      static_cast<const __nv_bfloat16 *>(x), perm, L, B, N, aug, query_side, beta);
+template <int D, int BK>
+static cudaError_t launch_stats(const SelectArgs &a, int64_t bh, int N, float *aug_q, float *aug_k,
+                                cudaStream_t st) {
+  const size_t smem = 2 * BK * D * 2 + kStatsBlocksPerCta * BK * sizeof(int);
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(k_block_stats<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const dim3 grid((N + kStatsBlocksPerCta - 1) / kStatsBlocksPerCta, static_cast<unsigned>(bh), 2);
+  k_block_stats<D, BK><<<grid, kStatsThreads, smem, st>>>(
+      static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k), a.perm_q,
+      a.perm_k, a.seqlen, N, aug_q, aug_k, a.beta);
   return cudaGetLastError();
 }
 
@@ -437,62 +662,63 @@ cudaError_t run_select(const SelectArgs &a, cudaStream_t st) {
                       : reinterpret_cast<float *>(ws + 2 * plan.keys_bytes + 2 * plan.aug_bytes);
   cudaError_t e;
 
-  // steps 1-2: norms and sort, per sorted tensor; identity otherwise
-  const void *srcs[2] = {a.q, a.k};
-  int32_t *perms[2] = {a.perm_q, a.perm_k};
-  const bool sorted[2] = {sort_q, sort_k};
-  int slot = 0;
-  for (int t = 0; t < 2; ++t) {
-    if (!sorted[t]) {
-      k_iota<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(perms[t], rows, L);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      continue;
-    }
-    uint64_t *k0 = keys0 + slot * rows;
-    uint64_t *k1 = keys1 + slot * rows;
-    ++slot;
-    const int tpr = D / 8;
-    const int64_t threads = rows * tpr;
-    const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-    if (D == 128)
-      k_sqnorm_keys<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(srcs[t]), k0,
-                                               rows, L);
-    else
-      k_sqnorm_keys<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(srcs[t]), k0,
-                                              rows, L);
+  // steps 1-2: norms and sort of the sorted tensors (one launch each for
+  // both); identity permutations otherwise
+  const void *srcs[2];
+  int32_t *perms[2];
+  int nsorted = 0;
+  if (sort_q) { srcs[nsorted] = a.q; perms[nsorted++] = a.perm_q; }
+  if (sort_k) { srcs[nsorted] = a.k; perms[nsorted++] = a.perm_k; }
+  if (!sort_q) {
+    k_iota<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(a.perm_q, rows, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // the chunk sort reads k0 and writes k1; merges ping-pong k1 <-> k0
-    if ((e = sort_sequences(k0, k1, k0, perms[t], static_cast<int>(bh), L, a.sort_window, st)) !=
+  }
+  if (!sort_k) {
+    k_iota<<<static_cast<unsigned>((rows + 255) / 256), 256, 0, st>>>(a.perm_k, rows, L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (nsorted > 0) {
+    const int rows_per_cta = (256 / (D / 8)) * kNormRowsPerThread;
+    const dim3 grid(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), nsorted);
+    const __nv_bfloat16 *x0 = static_cast<const __nv_bfloat16 *>(srcs[0]);
+    const __nv_bfloat16 *x1 = static_cast<const __nv_bfloat16 *>(srcs[nsorted - 1]);
+    if (D == 128)
+      k_sqnorm_keys<128><<<grid, 256, 0, st>>>(x0, x1, keys0, rows, L);
+    else
+      k_sqnorm_keys<64><<<grid, 256, 0, st>>>(x0, x1, keys0, rows, L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the chunk sort reads keys0 and writes keys1; merges ping-pong keys1 <-> keys0
+    if ((e = sort_sequences(keys0, keys1, keys0, perms[0], perms[nsorted - 1],
+                            static_cast<int>(nsorted * bh), bh, L, a.sort_window, st)) !=
         cudaSuccess)
       return e;
   }
 
-  // steps 3-4: statistics on the (possibly) permuted blocks
-  if (D == 128) {
-    if ((e = launch_stats<128>(a.q, a.perm_q, bh, L, B, N, aug_q, 1, a.beta, st))) return e;
-    if ((e = launch_stats<128>(a.k, a.perm_k, bh, L, B, N, aug_k, 0, a.beta, st))) return e;
-  } else {
-    if ((e = launch_stats<64>(a.q, a.perm_q, bh, L, B, N, aug_q, 1, a.beta, st))) return e;
-    if ((e = launch_stats<64>(a.k, a.perm_k, bh, L, B, N, aug_k, 0, a.beta, st))) return e;
-  }
+  // steps 3-4: statistics on the (possibly) permuted blocks, Q and K together
+  if (D == 128 && B == 128) e = launch_stats<128, 128>(a, bh, N, aug_q, aug_k, st);
+  else if (D == 128 && B == 64) e = launch_stats<128, 64>(a, bh, N, aug_q, aug_k, st);
+  else if (D == 64 && B == 128) e = launch_stats<64, 128>(a, bh, N, aug_q, aug_k, st);
+  else e = launch_stats<64, 64>(a, bh, N, aug_q, aug_k, st);
+  if (e != cudaSuccess) return e;
 
   // steps 5-7: scores (the compensation terms are skipped when beta == 0:
   // they are exact zeros then)
   const int ks = (a.beta == 0.f) ? D : 3 * D;
-  k_scores<<<dim3((N + 63) / 64, (N + 63) / 64, static_cast<unsigned>(bh)), 256, 0, st>>>(
+  k_scores<<<dim3((N + 127) / 128, (N + 127) / 128, static_cast<unsigned>(bh)), 256, 0, st>>>(
       aug_q, aug_k, scores, N, ks, 3 * D);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  // steps 8-11: top-kappa
+  // steps 8-11: top-kappa (keys of a row in registers: 32 * KPL >= N)
   const int64_t qrows = bh * N;
-  const size_t smem = static_cast<size_t>(kTopkWarps) * N * sizeof(uint32_t);
-  if (smem > 48 * 1024) {
-    if ((e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem))) != cudaSuccess)
-      return e;
-  }
-  k_topk<<<static_cast<unsigned>((qrows + kTopkWarps - 1) / kTopkWarps), kTopkWarps * 32, smem,
-           st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+  const unsigned tgrid = static_cast<unsigned>((qrows + kTopkWarps - 1) / kTopkWarps);
+  if (N <= 256)
+    k_topk<8><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+  else if (N <= 512)
+    k_topk<16><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+  else if (N <= 1024)
+    k_topk<32><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+  else
+    k_topk<128><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
   return cudaGetLastError();
 }
 
