@@ -65,16 +65,17 @@ def select_bytes(w, sort_q=True, sort_k=True):
 
 def launches_per_step(w):
     """Kernels the library launches per step (select + sparse attention) for
-    sort mode QK: per sorted tensor 1 norm pass, 1 chunk sort and
-    ceil(log2(L / 4096)) merge passes; 2 statistics, 1 score and 1 top-kappa
-    kernel; then 2 row gathers (Q, and K with V) and the attention kernel."""
+    sort mode QK: a norm pass, a chunk sort and ceil(log2(L / 4096)) merge
+    passes (Q and K together in each), one statistics, one score and one
+    top-kappa kernel; then one row-gather kernel (Q, K, V) and the attention
+    kernel."""
     passes = 0
     width = 4096
     while width < w.seqlen:
         width *= 2
         passes += 1
-    select = 2 * (2 + passes) + 2 + 1 + 1
-    attn = 2 + 1
+    select = 2 + passes + 3
+    attn = 2
     return select + attn
 
 

@@ -484,27 +484,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// row gather: out[bh, r, :] = in[bh, perm[bh, r], :]   (K and V share perm_k)
+// row gathers in one launch: out[job][bh, r, :] = in[job][bh, perm[job][bh, r], :]
+// (Q through pi_q; K and V through pi_k).  grid = (.., jobs); each thread
+// moves 16 bytes of kGatherRows rows, all loads in flight before the stores.
 // ---------------------------------------------------------------------------
+constexpr int kGatherRows = 4;
+
+struct GatherJobs {
+  const __nv_bfloat16 *in[3];
+  __nv_bfloat16 *out[3];
+  const int32_t *perm[3];
+};
+
 template <int D>
-__global__ void __launch_bounds__(256) k_permute_rows(const __nv_bfloat16 *__restrict__ in0,
-                                                      const __nv_bfloat16 *__restrict__ in1,
-                                                      const int32_t *__restrict__ perm,
-                                                      __nv_bfloat16 *__restrict__ out0,
-                                                      __nv_bfloat16 *__restrict__ out1,
-                                                      int64_t rows, int L) {
+__global__ void __launch_bounds__(256) k_gather_rows(const GatherJobs jobs, int64_t rows, int L) {
   constexpr int VPR = D / 8;
-  const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t row = gid / VPR;
-  const int c = static_cast<int>(gid % VPR);
-  if (row >= rows) return;
-  const int64_t bh = row / L;
-  const int64_t src = bh * L + __ldg(perm + row);
-  reinterpret_cast<uint4 *>(out0 + row * D)[c] =
-      __ldg(reinterpret_cast<const uint4 *>(in0 + src * D) + c);
-  if (in1 != nullptr)
-    reinterpret_cast<uint4 *>(out1 + row * D)[c] =
-        __ldg(reinterpret_cast<const uint4 *>(in1 + src * D) + c);
+  constexpr int RPW = 256 / VPR;
+  const int job = blockIdx.y;
+  const __nv_bfloat16 *in = jobs.in[job];
+  __nv_bfloat16 *out = jobs.out[job];
+  const int32_t *perm = jobs.perm[job];
+  const int c = threadIdx.x % VPR;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPW * kGatherRows + threadIdx.x / VPR;
+  int64_t src[kGatherRows];
+#pragma unroll
+  for (int u = 0; u < kGatherRows; ++u) {
+    const int64_t row = row0 + u * RPW;
+    src[u] = (row < rows) ? (row / L) * L + __ldg(perm + row) : -1;
+  }
+  uint4 v[kGatherRows];
+#pragma unroll
+  for (int u = 0; u < kGatherRows; ++u)
+    if (src[u] >= 0) v[u] = __ldg(reinterpret_cast<const uint4 *>(in + src[u] * D) + c);
+#pragma unroll
+  for (int u = 0; u < kGatherRows; ++u)
+    if (src[u] >= 0) reinterpret_cast<uint4 *>(out + (row0 + u * RPW) * D)[c] = v[u];
 }
 
 // ---------------------------------------------------------------------------
@@ -553,36 +567,36 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   unsigned char *ws = static_cast<unsigned char *>(a.workspace);
   const size_t t = align256(static_cast<size_t>(rows) * D * 2);
   cudaError_t e;
+  GatherJobs jobs;
+  int njobs = 0;
   if (a.perm_q) {
     __nv_bfloat16 *qp = reinterpret_cast<__nv_bfloat16 *>(ws);
     ws += t;
-    const int64_t threads = rows * (D / 8);
-    const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-    if (D == 128)
-      k_permute_rows<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.q), nullptr,
-                                                a.perm_q, qp, nullptr, rows, L);
-    else
-      k_permute_rows<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.q), nullptr,
-                                               a.perm_q, qp, nullptr, rows, L);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    jobs.in[njobs] = static_cast<const __nv_bfloat16 *>(a.q);
+    jobs.out[njobs] = qp;
+    jobs.perm[njobs++] = a.perm_q;
     qs = qp;
   }
   if (a.perm_k) {
     __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(ws);
     __nv_bfloat16 *vp = reinterpret_cast<__nv_bfloat16 *>(ws + t);
-    const int64_t threads = rows * (D / 8);
-    const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
-    if (D == 128)
-      k_permute_rows<128><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.k),
-                                                static_cast<const __nv_bfloat16 *>(a.v), a.perm_k,
-                                                kp, vp, rows, L);
-    else
-      k_permute_rows<64><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(a.k),
-                                               static_cast<const __nv_bfloat16 *>(a.v), a.perm_k,
-                                               kp, vp, rows, L);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    jobs.in[njobs] = static_cast<const __nv_bfloat16 *>(a.k);
+    jobs.out[njobs] = kp;
+    jobs.perm[njobs++] = a.perm_k;
+    jobs.in[njobs] = static_cast<const __nv_bfloat16 *>(a.v);
+    jobs.out[njobs] = vp;
+    jobs.perm[njobs++] = a.perm_k;
     ks = kp;
     vs = vp;
+  }
+  if (njobs > 0) {
+    const int rows_per_cta = (256 / (D / 8)) * kGatherRows;
+    const dim3 grid(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), njobs);
+    if (D == 128)
+      k_gather_rows<128><<<grid, 256, 0, st>>>(jobs, rows, L);
+    else
+      k_gather_rows<64><<<grid, 256, 0, st>>>(jobs, rows, L);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   alignas(64) CUtensorMap mq, mk, mv;
   if ((e = encode_tensor_map_3d(&mq, qs, D, L, bh, 64, kTileM)) != cudaSuccess) return e;
