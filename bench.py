@@ -46,6 +46,23 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
+# DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
+# of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
+# for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
+ATTN_TRAFFIC = {"ultra64k": dict(bytes=1737615360, kernel_sha="c5d3a8694e4c3f9c")}
+
+
+def attn_traffic(workload: str):
+    rec = ATTN_TRAFFIC.get(workload)
+    if rec is None:
+        return None
+    import hashlib
+    path = os.path.join(ROOT, "block_sparse_bidirectional_gb300", "csrc", "ba_attn.cu")
+    with open(path, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["bytes"] if sha == rec["kernel_sha"] else None
+
+
 def dense_flops(w):
     return 4.0 * w.batch * w.heads * w.seqlen * w.seqlen * w.head_dim
 
@@ -357,7 +374,7 @@ def main():
         warmup=args.warmup, ms_per_step=round(ms_step, 4), higher_is_better=True, scaling="weak",
         vs_baseline=None, dtype="bf16", data="synthetic", config=workload_config(w),
         roofline=dict(bound="tensor", achieved=round(att_tflops, 2), peak=pk["bf16"], unit="TFLOP/s",
-                      frac=round(att_tflops / pk["bf16"], 4), traffic=None,
+                      frac=round(att_tflops / pk["bf16"], 4), traffic=attn_traffic(w.name),
                       kernel="ba_sparse_attn (row gathers + tcgen05 attention kernel)",
                       peak_kind=f"bf16 dense burst, {pk['source']}",
                       algorithmic_flops_per_launch=attn_flops),
