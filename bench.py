@@ -63,6 +63,38 @@ def attn_traffic(workload: str):
     return rec["bytes"] if sha == rec["kernel_sha"] else None
 
 
+# ---- multi-GPU: one process per GPU, each on its own batch (weak scaling) ----
+# Every (batch, head) is independent in every step of the path, so ranks
+# exchange nothing on the data path: they meet at a barrier around the timed
+# region and reduce their elapsed times with a max.
+
+def rank_seed(w, rank: int) -> int:
+    """Each rank draws its own batch of the workload."""
+    return w.seed + rank
+
+
+def rank_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks_of(x: float, world: int, device) -> float:
+    """The slowest rank's time (the whole job ends when it does)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Aggregate throughput: every rank's work over the max-over-ranks time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dense_flops(w):
     return 4.0 * w.batch * w.heads * w.seqlen * w.seqlen * w.head_dim
 
@@ -250,19 +282,14 @@ def main():
     dev = torch.device("cuda", local)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world)
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks_of(x, world, dev)
 
     w = workloads.get(args.workload)
     kappa = w.kappa()
-    q, k, v, _ = workloads.make_inputs(w, seed=w.seed + rank)
+    q, k, v, _ = workloads.make_inputs(w, seed=rank_seed(w, rank))
     b, h, L, d, B = w.batch, w.heads, w.seqlen, w.head_dim, w.block
     N = w.nblocks
     bsb.load()
@@ -365,7 +392,7 @@ def main():
 
     pk = peaks()
     flops_step = dense_flops(w)
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, ms_step)
     att_tflops = attn_flops / (att_ms * 1e-3) / 1e12
     sel_b = select_bytes(w)
     sel_gbs = sel_b / (sel_ms * 1e-3) / 1e9
@@ -378,7 +405,7 @@ def main():
                       kernel="ba_sparse_attn (row gathers + tcgen05 attention kernel)",
                       peak_kind=f"bf16 dense burst, {pk['source']}",
                       algorithmic_flops_per_launch=attn_flops),
-        e2e=dict(value=round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 3), unit=UNIT,
+        e2e=dict(value=round(whole_job_tflops(world, flops_step, e2e_ms), 3), unit=UNIT,
                  ms_per_step=round(e2e_ms, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
         gpu_launches=launches_per_step(w) * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
