@@ -20,7 +20,8 @@ import re
 from . import _build
 
 __all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_sparse_attn", "ba_sparse_attn_into",
-           "ba_attn_dense", "ba_attn_dense_into", "last_device_error", "BAError",
+           "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
+           "last_device_error", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
            "sparse_attn_workspace_size", "header_functions", "LIB_PATH"]
 
@@ -42,6 +43,7 @@ _SIGS = {
                        + [_c_void_p] * 3 + [_c_size, _c_void_p]),
     "ba_attn_dense": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [_c_float] + [_c_void_p] * 3),
     "ba_last_device_error": (_c_int, [_c_void_p, _c_u32p]),
+    "ba_merge_lse": (_c_int, [_c_void_p] * 4 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
     "ba_select_noalloc": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int]
                           + [_c_void_p] * 5 + [_c_void_p]),
 }
@@ -220,6 +222,26 @@ def ba_attn_dense(q, k, v, scale=0.0):
     o = torch.empty_like(q)
     lse = torch.empty((b, h, L), dtype=torch.float32, device=q.device)
     ba_attn_dense_into(q, k, v, scale, o, lse)
+    return o, lse
+
+
+def ba_merge_lse_into(o1, lse1, o2, lse2, o, lse):
+    """Merge two results over disjoint key sets (LoSA merge); writes o, lse."""
+    lib = load()
+    _need_cuda(o1, lse1, o2, lse2, o, lse)
+    d = o1.shape[-1]
+    rows = o1.numel() // d
+    st = lib.ba_merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), rows, d, _ptr(o), _ptr(lse),
+                          _stream(o1.device))
+    _check(st, "ba_merge_lse")
+
+
+def ba_merge_lse(o1, lse1, o2, lse2):
+    """Returns (o, lse) of the merged result; o1/o2 bf16 [..., d], lse fp32 [...]."""
+    torch = _torch()
+    o = torch.empty_like(o1)
+    lse = torch.empty_like(lse1)
+    ba_merge_lse_into(o1, lse1, o2, lse2, o, lse)
     return o, lse
 
 

@@ -145,7 +145,7 @@ size_t ba_sparse_attn_workspace_size(int batch, int heads, int seqlen, int head_
                                      int kappa, int has_perm_q, int has_perm_k) {
   (void)kappa;
   if (check_shape(batch, heads, seqlen, head_dim, block) != BA_OK) return 0;
-  return attn_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim,
+  return attn_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim, block,
                               has_perm_q != 0, has_perm_k != 0);
 }
 
@@ -209,6 +209,20 @@ int ba_attn_dense(const void *q, const void *k, const void *v, int batch, int he
   a.o = o;
   a.lse = lse;
   return map_cuda(run_attention(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ba_merge_lse(const void *o1, const float *lse1, const void *o2, const float *lse2,
+                 int64_t rows, int head_dim, void *o, float *lse, ba_stream_t stream) {
+  if (rows < 0) return BA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return BA_ERR_UNSUPPORTED;
+  if (rows == 0) return BA_OK;
+  if (!o1 || !lse1 || !o2 || !lse2 || !o || !lse) return BA_ERR_INVALID_ARG;
+  if (!aligned16(o1) || !aligned16(o2) || !aligned16(o) || !aligned16(lse1) || !aligned16(lse2) ||
+      !aligned16(lse))
+    return BA_ERR_INVALID_ARG;
+  if (rows >= (static_cast<int64_t>(1) << 40) / head_dim) return BA_ERR_UNSUPPORTED;
+  return map_cuda(run_merge_lse(o1, lse1, o2, lse2, rows, head_dim, o, lse,
+                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int ba_last_device_error(ba_stream_t stream, uint32_t *detail) {

@@ -74,7 +74,7 @@ struct AttnLayout {
   static constexpr int kG = kTileM / BK;               // query blocks per tile
   static constexpr int kQBytes = kTileM * D * 2;       // one Q tile
   static constexpr int kSlotBytes = BK * D * 2;        // one K or V block
-  static constexpr int kListBytes = (kG > 1) ? kTiles * kMaxBlocks * 2 : 0;
+  static constexpr int kListBytes = 0;  // tile lists are read from global memory
   static constexpr int kBarBytes = 512;
   static constexpr int kMaxDyn = 227 * 1024;
   static constexpr int kSlots =
@@ -99,7 +99,9 @@ struct AttnParams {
   int N;          // key blocks (and query blocks) of size BK
   int kappa;      // list length per query block (unused when dense)
   int n_tiles;    // 128-row query tiles per sequence
-  const int32_t *block_idx;
+  int npairs;     // CTAs (tile pairs) per sequence
+  const uint16_t *pair_lists;  // [b*h][npairs][2][N]: per tile, common blocks first
+  const int32_t *pair_counts;  // [b*h][npairs][4]: n0, n1, common, -
   const int32_t *perm_q;  // sorted query position -> original row (nullable)
   __nv_bfloat16 *o;
   float *lse;
@@ -107,28 +109,21 @@ struct AttnParams {
 };
 
 // A key-block entry: bits 0-11 block id, bit 12+g set when query block g of
-// the tile selected it.
-template <int G, bool kDense>
-__device__ __forceinline__ uint32_t entry_at(const AttnParams &p, const uint16_t *list,
-                                             const int32_t *idx, int j) {
-  if (kDense) return static_cast<uint32_t>(j) | (3u << 12);
-  if (G == 1) return static_cast<uint32_t>(min(max(__ldg(idx + j), 0), p.N - 1)) | (1u << 12);
-  return list[j];
-}
+// the tile selected it.  Sparse tiles read their entries from the pair list
+// (k_pair_lists); dense tiles walk every block.
+__device__ __forceinline__ uint32_t dense_entry(int j) { return static_cast<uint32_t>(j) | (3u << 12); }
 
 template <int D, int BK, bool kDense>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Lay = AttnLayout<D, BK>;
-  constexpr int G = Lay::kG;
   constexpr int S = Lay::kSlots;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sQ = smem + Lay::kOffQ;
   uint8_t *sSlot = smem + Lay::kOffSlots;
-  uint16_t *lists = reinterpret_cast<uint16_t *>(smem + Lay::kOffList);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Lay::kOffBar);
   uint64_t *q_full = bars;
   uint64_t *slot_full = bars + 1;
@@ -137,7 +132,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t *p_full = s_full + kTiles;  // [kTiles]
   uint64_t *o_done = p_full + kTiles;  // [kTiles]
   uint64_t *drain = o_done + kTiles;
-  uint32_t *misc = reinterpret_cast<uint32_t *>(drain + 1);  // tmem, n0, n1, abort
+  uint32_t *misc = reinterpret_cast<uint32_t *>(drain + 1);  // tmem, n0, n1, abort, common
   volatile int *abort_flag = reinterpret_cast<volatile int *>(&misc[3]);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -156,8 +151,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
-    misc[1] = misc[2] = 0;
-    misc[3] = 0;
+    misc[3] = 0;  // abort flag; misc[1], misc[2], misc[4] are the counts below
     fence_barrier_init();
     fence_proxy_async_smem();
   }
@@ -166,72 +160,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_before();
   }
 
-  // ---- per-tile key-block lists ------------------------------------------
-  if (kDense || G == 1) {
-    if (threadIdx.x < kTiles) {
-      const int tile = tile0 + threadIdx.x;
-      misc[1 + threadIdx.x] = (tile < p.n_tiles) ? (kDense ? p.N : p.kappa) : 0;
+  // ---- per-tile entry counts ----------------------------------------------
+  const int pair = blockIdx.x;
+  const uint16_t *plist[kTiles];
+  for (int t = 0; t < kTiles; ++t)
+    plist[t] = kDense ? nullptr
+                      : p.pair_lists + ((static_cast<int64_t>(bh) * p.npairs + pair) * kTiles + t) * p.N;
+  if (threadIdx.x <= kTiles) {
+    if (kDense) {
+      if (threadIdx.x < kTiles)
+        misc[1 + threadIdx.x] = (tile0 + static_cast<int>(threadIdx.x) < p.n_tiles) ? p.N : 0;
+    } else {
+      const int32_t *cnt = p.pair_counts + (static_cast<int64_t>(bh) * p.npairs + pair) * 4;
+      misc[threadIdx.x < kTiles ? 1 + threadIdx.x : 4] = cnt[threadIdx.x];
     }
-  } else {
-    // G == 2: per tile, the union of its two query blocks' lists, ascending,
-    // each entry tagged with which of the two selected it.
-    constexpr int kWords = kMaxBlocks / 32;
-    uint32_t *bitmap = reinterpret_cast<uint32_t *>(sSlot);  // scratch, before any load
-    const int nwords = (p.N + 31) / 32;
-    for (int i = threadIdx.x; i < kTiles * G * kWords; i += kAttnThreads) bitmap[i] = 0u;
-    __syncthreads();
-    for (int t = 0; t < kTiles; ++t)
-      for (int g = 0; g < G; ++g) {
-        const int gq = (tile0 + t) * G + g;
-        if (gq >= p.N) continue;
-        const int32_t *src = p.block_idx + (static_cast<int64_t>(bh) * p.N + gq) * p.kappa;
-        for (int i = threadIdx.x; i < p.kappa; i += kAttnThreads) {
-          const int blk = src[i];
-          if (blk < 0 || blk >= p.N) continue;  // ids are not validated on the host
-          atomicOr(&bitmap[(t * G + g) * kWords + (blk >> 5)], 1u << (blk & 31));
-        }
-      }
-    __syncthreads();
-    if (warp < kTiles) {
-      const int t = warp;
-      uint16_t *list = lists + t * kMaxBlocks;
-      int base = 0;
-      for (int w0 = 0; w0 < nwords; w0 += 32) {
-        const int w = w0 + lane;
-        const uint32_t m0 = (w < nwords) ? bitmap[(t * G + 0) * kWords + w] : 0u;
-        const uint32_t m1 = (w < nwords) ? bitmap[(t * G + 1) * kWords + w] : 0u;
-        uint32_t u = m0 | m1;
-        const int cnt = __popc(u);
-        int incl = cnt;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, off);
-          if (lane >= off) incl += v;
-        }
-        int pos = base + incl - cnt;
-        while (u) {
-          const int b = __ffs(u) - 1;
-          u &= u - 1;
-          const uint32_t sel = ((m0 >> b) & 1u) | (((m1 >> b) & 1u) << 1);
-          list[pos++] = static_cast<uint16_t>((w * 32 + b) | (sel << 12));
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
-      }
-      if (lane == 0) misc[1 + t] = base;
-    }
-    // the bitmap scratch is overwritten by TMA (async proxy) later
-    fence_proxy_async_smem();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const int n_t[kTiles] = {static_cast<int>(misc[1]), static_cast<int>(misc[2])};
   const int nmax = max(n_t[0], n_t[1]);
-  // dense: both tiles walk the same blocks, so every K/V load serves both
-  const bool shared = kDense && n_t[1] > 0;
-  const int32_t *idx_t[kTiles];
-  for (int t = 0; t < kTiles; ++t)
-    idx_t[t] = p.block_idx + (static_cast<int64_t>(bh) * p.N + (tile0 + t)) * p.kappa;
+  // Positions j < n_common hold the same block in both tiles' lists (dense:
+  // every position), so the K_j / V_j load is shared by the two tiles there.
+  const int n_common = kDense ? (n_t[1] > 0 ? n_t[0] : 0) : static_cast<int>(misc[4]);
 
   if (warp < 4) {
     reg_dealloc<kRegsLow>();
@@ -252,7 +203,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       int issued = 0;
       auto load = [&](bool is_v, int t, int j) -> bool {
-        const int blk = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j) & 0xFFF;
+        const int blk = kDense ? j : (plist[t][j] & 0xFFF);
         const int s = issued % S;
         if (issued >= S && !mbar_wait(&slot_empty[s], ((issued / S) & 1) ^ 1u, kSiteKEmpty, abort_flag))
           return false;
@@ -267,12 +218,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // the same operand order in which the MMA thread consumes the slots
       bool ok = true;
       for (int t = 0; ok && t < kTiles; ++t)
-        if (n_t[t] > 0 && !(shared && t == 1)) ok = load(false, t, 0);
+        if (n_t[t] > 0 && !(t == 1 && 0 < n_common)) ok = load(false, t, 0);
       for (int j = 0; ok && j < nmax; ++j)
         for (int t = 0; ok && t < kTiles; ++t) {
-          if (j >= n_t[t] || (shared && t == 1)) continue;
-          ok = load(true, t, j);
-          if (ok && j + 1 < n_t[t]) ok = load(false, t, j + 1);
+          if (j >= n_t[t]) continue;
+          if (!(t == 1 && j < n_common)) ok = load(true, t, j);
+          if (ok && j + 1 < n_t[t] && !(t == 1 && j + 1 < n_common)) ok = load(false, t, j + 1);
         }
       // drain: the last copy issued into each slot has landed
       mbar_wait_drain(q_full, 0);
@@ -315,13 +266,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                       (j > 0 || ks > 0) ? 1u : 0u);
         }
       };
-      int slot_k0 = 0, slot_v0 = 0;  // dense: slots loaded for tile 0, reused by tile 1
+      int slot_k0 = 0, slot_v0 = 0;  // shared positions: slots loaded for tile 0, reused by tile 1
       for (int t = 0; ok && t < kTiles; ++t) {
         if (n_t[t] == 0) continue;
+        const bool sh = 0 < n_common;
         int sl = slot_k0;
-        if (!(shared && t == 1) && !(ok = take(sl))) break;
+        if (!(sh && t == 1) && !(ok = take(sl))) break;
         mma_s(t, sl);
-        if (!shared || t == 1) mma_commit(&slot_empty[sl]);
+        if (!sh || t == 1) mma_commit(&slot_empty[sl]);
         else slot_k0 = sl;
       }
       for (int j = 0; ok && j < nmax; ++j) {
@@ -329,17 +281,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if (j >= n_t[t]) continue;
           if (!(ok = mbar_wait(&p_full[t], j & 1, kSitePFull, abort_flag))) break;
           tc_fence_after();
+          const bool shv = j < n_common;
           int sv = slot_v0;
-          if (!(shared && t == 1) && !(ok = take(sv))) break;
+          if (!(shv && t == 1) && !(ok = take(sv))) break;
           mma_pv(t, sv, j);
           if (j + 1 == n_t[t]) mma_commit(&o_done[t]);
-          if (!shared || t == 1) mma_commit(&slot_empty[sv]);
+          if (!shv || t == 1) mma_commit(&slot_empty[sv]);
           else slot_v0 = sv;
           if (j + 1 < n_t[t]) {
+            const bool shk = j + 1 < n_common;
             int sk = slot_k0;
-            if (!(shared && t == 1) && !(ok = take(sk))) break;
+            if (!(shk && t == 1) && !(ok = take(sk))) break;
             mma_s(t, sk);
-            if (!shared || t == 1) mma_commit(&slot_empty[sk]);
+            if (!shk || t == 1) mma_commit(&slot_empty[sk]);
             else slot_k0 = sk;
           }
         }
@@ -362,17 +316,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint64_t cl2 = f2_pack(cl, cl);
     float m = -INFINITY;
     uint64_t l2 = f2_pack(0.f, 0.f);  // running sum of the fp32 weights (two halves)
+    // Sum of the bf16 rounding errors of every block's largest weight: the O
+    // normaliser l + lcorr matches the weights the PV product consumed for
+    // the terms that dominate a row (a row's largest weight is some block's
+    // largest), so a row that attends to one key returns that key's value.
+    float lcorr = 0.f;
     bool ok = true;
     const int n = n_t[t];
-    int my_blk = 0;  // sparse, one query block per tile: 32 list entries, one per lane
+    uint32_t my_e = 0;  // sparse: 32 list entries at a time, one per lane
     for (int j = 0; j < n; ++j) {
       uint32_t e;
-      if (!kDense && G == 1) {
-        if ((j & 31) == 0)
-          my_blk = (j + lane < n) ? min(max(__ldg(idx_t[t] + j + lane), 0), p.N - 1) : 0;
-        e = static_cast<uint32_t>(__shfl_sync(0xffffffffu, my_blk, j & 31)) | (1u << 12);
+      if (!kDense) {
+        if ((j & 31) == 0) my_e = (j + lane < n) ? __ldg(plist[t] + j + lane) : 0u;
+        e = __shfl_sync(0xffffffffu, my_e, j & 31);
       } else {
-        e = entry_at<G, kDense>(p, lists + t * kMaxBlocks, idx_t[t], j);
+        e = dense_entry(j);
       }
       const int blk = e & 0xFFF;
       const bool sel = (e >> (12 + my_g)) & 1u;
@@ -401,6 +359,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         alpha = resc ? fast_exp2(m - m_new) : 0.f;
         const uint64_t a2 = f2_pack(alpha, alpha), z2 = f2_pack(0.f, 0.f);
         l2 = f2_fma(l2, a2, z2);
+        lcorr *= alpha;
         m = m_new;
       }
       // lazy rescale of O_t: PV_{j-1} has completed (it was issued before
@@ -419,6 +378,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       const float nm = (m == -INFINITY) ? 0.f : -m;
       const uint64_t nm2 = f2_pack(nm, nm);
+      {
+        // computed exactly as this element's P entry below (same fma, ex2, RN)
+        const float pbm = fast_exp2(fmaf(mx, cl, nm));
+        lcorr += __bfloat162float(__float2bfloat16_rn(pbm)) - pbm;
+      }
       // P_j overwrites the first BK/2 columns of S_j (bf16 pairs), 32 at a time
 #pragma unroll
       for (int h = 0; h < BK / 64; ++h) {
@@ -451,7 +415,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int64_t orig =
           row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted] : row_sorted)
                     : 0;
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      const float lo = l + lcorr;
+      const float inv = (lo > 0.f) ? 1.f / lo : 0.f;
       uint4 *orow = reinterpret_cast<uint4 *>(p.o + (static_cast<int64_t>(bh) * p.L + orig) * D);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -522,6 +487,98 @@ __global__ void __launch_bounds__(256) k_gather_rows(const GatherJobs jobs, int6
 }
 
 // ---------------------------------------------------------------------------
+// tile-pair lists.  For each CTA (two 128-row query tiles) and each of its
+// tiles: the key blocks the tile's query blocks selected (for B = 64 the
+// union of two lists, each entry tagged with which query block selected it),
+// ordered with the blocks both tiles selected first -- in the same order in
+// both lists, so the attention kernel loads them once for both tiles -- then
+// the tile's other blocks; ascending within each part.  (Online softmax does
+// not depend on the order of the key blocks.)  One warp per pair.
+// ---------------------------------------------------------------------------
+constexpr int kPairWarps = 4;
+constexpr int kPairWords = kMaxBlocks / 32;
+
+template <int G>
+__global__ void __launch_bounds__(kPairWarps * 32) k_pair_lists(
+    const int32_t *__restrict__ idx, int N, int kappa, int n_tiles, int npairs, int64_t total,
+    uint16_t *__restrict__ lists, int32_t *__restrict__ counts) {
+  __shared__ uint32_t bm[kPairWarps][kTiles][G][kPairWords];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t gp = static_cast<int64_t>(blockIdx.x) * kPairWarps + warp;
+  if (gp >= total) return;  // warp-uniform; no block barrier below
+  const int64_t bh = gp / npairs;
+  const int pair = static_cast<int>(gp % npairs);
+  const int nwords = (N + 31) / 32;
+  uint32_t(*b)[G][kPairWords] = bm[warp];
+  for (int t = 0; t < kTiles; ++t)
+    for (int g = 0; g < G; ++g)
+      for (int w = lane; w < nwords; w += 32) b[t][g][w] = 0u;
+  __syncwarp();
+  for (int t = 0; t < kTiles; ++t) {
+    const int tile = pair * kTiles + t;
+    if (tile >= n_tiles) continue;
+    for (int g = 0; g < G; ++g) {
+      const int gq = tile * G + g;
+      if (gq >= N) continue;
+      const int32_t *src = idx + (bh * N + gq) * kappa;
+      for (int i = lane; i < kappa; i += 32) {
+        const int blk = __ldg(src + i);
+        if (blk < 0 || blk >= N) continue;  // ids are not validated on the host
+        atomicOr(&b[t][g][blk >> 5], 1u << (blk & 31));
+      }
+    }
+  }
+  __syncwarp();
+  uint16_t *out[kTiles] = {lists + (gp * kTiles) * N, lists + (gp * kTiles + 1) * N};
+  auto any = [&](int t, int w) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) m |= b[t][g][w];
+    return m;
+  };
+  auto entry = [&](int t, int w, int bit) {
+    uint32_t sel = 0u;
+#pragma unroll
+    for (int g = 0; g < G; ++g) sel |= ((b[t][g][w] >> bit) & 1u) << g;
+    return static_cast<uint16_t>((w * 32 + bit) | (sel << 12));
+  };
+  int common = 0, n[kTiles] = {0, 0};
+  // pass 0: blocks of both tiles; pass 1: tile 0 only; pass 2: tile 1 only
+  for (int pass = 0; pass < 3; ++pass) {
+    int pos = (pass == 0) ? 0 : common;
+    for (int w0 = 0; w0 < nwords; w0 += 32) {
+      const int w = w0 + lane;
+      const uint32_t a0 = (w < nwords) ? any(0, w) : 0u, a1 = (w < nwords) ? any(1, w) : 0u;
+      uint32_t m = (pass == 0) ? (a0 & a1) : (pass == 1) ? (a0 & ~a1) : (a1 & ~a0);
+      const int cnt = __popc(m);
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      int q = pos + incl - cnt;
+      while (m) {
+        const int bit = __ffs(m) - 1;
+        m &= m - 1;
+        if (pass != 2) out[0][q] = entry(0, w, bit);
+        if (pass != 1) out[1][q] = entry(1, w, bit);
+        ++q;
+      }
+      pos += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (pass == 0) common = pos;
+    else n[pass - 1] = pos;
+  }
+  if (lane == 0) {
+    counts[gp * 4 + 0] = n[0];
+    counts[gp * 4 + 1] = n[1];
+    counts[gp * 4 + 2] = common;
+    counts[gp * 4 + 3] = 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -533,9 +590,18 @@ cudaError_t take_attn_error_word(uint32_t *word) {
   return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(uint32_t));
 }
 
-size_t attn_workspace_bytes(int64_t bh, int L, int D, bool perm_q, bool perm_k) {
+// Workspace of the sparse call: Q' (perm_q), K' and V' (perm_k), then the
+// tile-pair lists and their counts.
+static size_t pair_list_bytes(int64_t bh, int L, int B) {
+  const int64_t n = (L + B - 1) / B;
+  const int64_t npairs = ((L + kTileM - 1) / kTileM + kTiles - 1) / kTiles;
+  return align256(static_cast<size_t>(bh * npairs * kTiles * n) * sizeof(uint16_t)) +
+         align256(static_cast<size_t>(bh * npairs * 4) * sizeof(int32_t));
+}
+
+size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool perm_k) {
   const size_t t = align256(static_cast<size_t>(bh) * L * D * 2);
-  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0);
+  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0) + pair_list_bytes(bh, L, B);
 }
 
 template <int D, int BK, bool kDense>
@@ -588,6 +654,26 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
     jobs.perm[njobs++] = a.perm_k;
     ks = kp;
     vs = vp;
+    ws += 2 * t;
+  }
+  uint16_t *pair_lists = nullptr;
+  int32_t *pair_counts = nullptr;
+  const int n_tiles = (L + kTileM - 1) / kTileM;
+  const int npairs = (n_tiles + kTiles - 1) / kTiles;
+  if (!dense) {
+    const int64_t nblk = (L + BK - 1) / BK;
+    pair_lists = reinterpret_cast<uint16_t *>(ws);
+    pair_counts = reinterpret_cast<int32_t *>(
+        ws + align256(static_cast<size_t>(bh * npairs * kTiles * nblk) * sizeof(uint16_t)));
+    const int64_t total = bh * npairs;
+    const unsigned grid = static_cast<unsigned>((total + kPairWarps - 1) / kPairWarps);
+    if (BK == 128)
+      k_pair_lists<1><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
+                                                        n_tiles, npairs, total, pair_lists, pair_counts);
+    else
+      k_pair_lists<2><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
+                                                        n_tiles, npairs, total, pair_lists, pair_counts);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (njobs > 0) {
     const int rows_per_cta = (256 / (D / 8)) * kGatherRows;
@@ -606,9 +692,10 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   AttnParams p;
   p.L = L;
   p.N = (L + BK - 1) / BK;
-  p.kappa = dense ? p.N : a.kappa;
-  p.n_tiles = (L + kTileM - 1) / kTileM;
-  p.block_idx = a.block_idx;
+  p.n_tiles = n_tiles;
+  p.npairs = npairs;
+  p.pair_lists = pair_lists;
+  p.pair_counts = pair_counts;
   p.perm_q = a.perm_q;
   p.o = static_cast<__nv_bfloat16 *>(a.o);
   p.lse = a.lse;

@@ -32,8 +32,11 @@ struct AttnArgs {
 size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode);
 cudaError_t run_select(const SelectArgs &a, cudaStream_t st);
 
-size_t attn_workspace_bytes(int64_t bh, int L, int D, bool perm_q, bool perm_k);
+size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool perm_k);
 cudaError_t run_attention(const AttnArgs &a, cudaStream_t st);
+
+cudaError_t run_merge_lse(const void *o1, const float *lse1, const void *o2, const float *lse2,
+                          int64_t rows, int head_dim, void *o, float *lse, cudaStream_t st);
 
 // Reads and clears the attention kernels' device error word (synchronous).
 cudaError_t take_attn_error_word(uint32_t *word);

@@ -185,6 +185,23 @@ int ba_attn_dense(const void *q, const void *k, const void *v, int batch,
                   float *lse, ba_stream_t stream);
 
 /*
+ * Merge of two attention results over DISJOINT key sets of the same rows, the
+ * online-softmax combination of the LoSA summary post ("merge and update":
+ * cached prefix attention joined with newly computed attention through the
+ * log-normaliser):
+ *     lse[r] = ln(exp(lse1[r]) + exp(lse2[r]))
+ *     o[r]   = exp(lse1[r] - lse[r]) o1[r] + exp(lse2[r] - lse[r]) o2[r]
+ * o1, o2, o   bf16 [rows, head_dim]; lse1, lse2, lse  fp32 [rows] (natural
+ *             log, as ba_sparse_attn writes them).  Device pointers; o may
+ *             be o1 or o2 and lse may be lse1 or lse2 (in place).
+ * A part with lse = -inf (no keys) has weight 0; when both are -inf the row
+ * gets o = 0, lse = -inf.  head_dim in {64, 128}; rows >= 0 (0: no-op).
+ */
+int ba_merge_lse(const void *o1, const float *lse1, const void *o2,
+                 const float *lse2, int64_t rows, int head_dim, void *o,
+                 float *lse, ba_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * kernels set when a bounded wait gives up.  Returns BA_OK,
  * BA_ERR_DEVICE_TIMEOUT or BA_ERR_CUDA.  `detail` (may be NULL) receives the

@@ -51,9 +51,15 @@ def test_workspace_sizes():
     assert lib.ba_select_workspace_size(b, h, L, d, B, 256, 0, 0) == 2 * aug + sc
     assert lib.ba_select_workspace_size(b, h, L, d, B, 256, 3, 0) == 2 * keys + 2 * aug + sc
     t = b * h * L * d * 2
-    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t
-    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t
-    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 0) == 0
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+    # tile-pair lists (uint16, two tiles of N entries per CTA) and their counts
+    npairs = ((L + 127) // 128 + 1) // 2
+    pl = a256(b * h * npairs * 2 * N * 2) + a256(b * h * npairs * 4 * 4)
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t + pl
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t + pl
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 0) == pl
     # unsupported shapes report 0
     assert lib.ba_select_workspace_size(1, 1, 1024, 96, 64, 8, 3, 0) == 0
     assert lib.ba_select_workspace_size(1, 1, 1024, 64, 32, 8, 3, 0) == 0
@@ -130,3 +136,12 @@ def test_no_cpu_path():
         bsb.ba_attn_dense(q, q, q)
     with pytest.raises(ValueError):
         bsb.ba_select(q, q, 64, 1)
+
+
+def test_merge_lse_rejects():
+    lib = bsb.load()
+    assert lib.ba_merge_lse(P, P, P, P, 0, 128, P, P, None) == OK          # no rows: no-op
+    assert lib.ba_merge_lse(P, P, P, P, -1, 128, P, P, None) == INVALID
+    assert lib.ba_merge_lse(P, P, P, P, 10, 96, P, P, None) == UNSUPPORTED
+    assert lib.ba_merge_lse(None, P, P, P, 10, 128, P, P, None) == INVALID
+    assert lib.ba_merge_lse(P, P, MIS, P, 10, 64, P, P, None) == INVALID

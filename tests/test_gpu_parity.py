@@ -211,3 +211,44 @@ def test_dense_full_size_sampled(dev):
 def test_device_error_word_clean(dev):
     st, word = bsb.last_device_error()
     assert st == 0 and word == 0
+
+
+def test_merge_lse_kernel_against_oracle(dev):
+    """ba_merge_lse (LoSA merge) against the oracle's merge on random partial
+    results, including rows whose key set was empty (LSE = -inf)."""
+    gen = torch.Generator().manual_seed(21)
+    for d in (64, 128):
+        rows = 3001
+        o1 = torch.randn((rows, d), generator=gen).to(torch.bfloat16)
+        o2 = torch.randn((rows, d), generator=gen).to(torch.bfloat16)
+        l1 = torch.randn(rows, generator=gen) * 4
+        l2 = torch.randn(rows, generator=gen) * 4
+        l1[::7] = -float("inf")
+        l2[::11] = -float("inf")
+        o, lse = bsb.ba_merge_lse(o1.to(dev), l1.to(dev), o2.to(dev), l2.to(dev))
+        torch.cuda.synchronize()
+        both = torch.isinf(l1) & torch.isinf(l2)
+        one = ~both.numpy()
+        # the merge is defined where at least one part has keys
+        om, lm = O.merge_lse(to64(o1)[one], l1.double().numpy()[one], to64(o2)[one],
+                             l2.double().numpy()[one])
+        og, lg = to64(o), lse.cpu().double().numpy()
+        # bf16 output: within one bf16 rounding of the fp64 merge
+        assert np.all(np.abs(og[one] - om) <= np.abs(om) * 2.0 ** -8 + 1e-6)
+        assert np.all(np.abs(lg[one] - lm) <= 1e-5 * np.maximum(1.0, np.abs(lm)))
+        assert np.all(og[both.numpy()] == 0) and np.all(np.isneginf(lg[both.numpy()]))
+
+
+def test_merge_lse_kernel_joins_split_lists(dev):
+    """Attention over the two halves of every list, merged on the GPU, equals
+    the single call over the whole list (within the attention tolerances)."""
+    q, k, v = workloads.random_inputs(1, 4, 4096, 128, seed=31)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    sel = bsb.ba_select(qd, kd, 128, 12, 1.0, 3)
+    idx = sel["block_idx"]
+    o, l = bsb.ba_sparse_attn(qd, kd, vd, 128, sel["perm_q"], sel["perm_k"], idx)
+    o1, l1 = bsb.ba_sparse_attn(qd, kd, vd, 128, sel["perm_q"], sel["perm_k"], idx[..., :5].contiguous())
+    o2, l2 = bsb.ba_sparse_attn(qd, kd, vd, 128, sel["perm_q"], sel["perm_k"], idx[..., 5:].contiguous())
+    om, lm = bsb.ba_merge_lse(o1, l1, o2, l2)
+    torch.cuda.synchronize()
+    check_attention(to64(om), lm.cpu().double().numpy(), to64(o), l.cpu().double().numpy())
