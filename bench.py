@@ -49,7 +49,7 @@ def peaks():
 # DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
 # of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
 # for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
-ATTN_TRAFFIC = {"ultra64k": dict(bytes=1737615360, kernel_sha="c5d3a8694e4c3f9c")}
+ATTN_TRAFFIC = {"ultra64k": dict(bytes=1722405376, kernel_sha="25daa684ca8dea8f")}
 
 
 def attn_traffic(workload: str):

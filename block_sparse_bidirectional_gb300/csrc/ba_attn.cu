@@ -46,8 +46,14 @@ namespace ba {
 constexpr int kTileM = 128;          // query rows per tile (TMEM lanes)
 constexpr int kTiles = 2;            // query tiles per CTA (ping-pong)
 constexpr int kAttnThreads = 384;    // 12 warps
-constexpr int kRegsLow = 72;         // warps 0-3 after setmaxnreg.dec
-constexpr int kRegsHigh = 216;       // warps 4-11 after setmaxnreg.inc (4*32*72 + 8*32*216 = 384*168)
+// Registers per thread after setmaxnreg: warps 0-3 drop to kLow, warps 4-11
+// rise to kHigh; 4*32*kLow + 8*32*kHigh must equal the launch's 384*168.
+// 64-key tiles hold more pointer state in the producer/MMA warps and fewer
+// S columns per softmax thread, so they split differently.
+template <int BK> struct RegSplit { static constexpr int kLow = 72, kHigh = 216; };
+template <> struct RegSplit<64> { static constexpr int kLow = 104, kHigh = 200; };
+static_assert(4 * 32 * RegSplit<128>::kLow + 8 * 32 * RegSplit<128>::kHigh == 384 * 168, "split");
+static_assert(4 * 32 * RegSplit<64>::kLow + 8 * 32 * RegSplit<64>::kHigh == 384 * 168, "split");
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxBlocks = 4096;
 
@@ -185,7 +191,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   const int n_common = kDense ? (n_t[1] > 0 ? n_t[0] : 0) : static_cast<int>(misc[4]);
 
   if (warp < 4) {
-    reg_dealloc<kRegsLow>();
+    reg_dealloc<RegSplit<BK>::kLow>();
     if (warp == 0 && lane == 0) {
       // ===================== TMA producer ===================================
       prefetch_tensormap(&tmQ);
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       mbar_wait_drain(drain, 0);
     }
   } else {
-    reg_alloc<kRegsHigh>();
+    reg_alloc<RegSplit<BK>::kHigh>();
     // ===================== softmax + epilogue, one warpgroup per tile =======
     const int t = (warp - 4) >> 2;
     const int r = threadIdx.x - 128 * (t + 1);

@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
                                                               int final_pass) {
   __shared__ uint64_t s_in[spad_size(kMergeTile)];
   __shared__ uint64_t s_out[spad_size(kMergeTile)];
-  __shared__ int s_split[2];
+  __shared__ int s_lo[2], s_hi[2], s_cnt[2];
   const int w = blockIdx.y;
   const int seq = blockIdx.z;
   const int wlen = window_len(g, w);
@@ -269,20 +269,41 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
   const uint64_t *B = in + base + a1;
   const int d0 = o_cta - p0;
   const int cnt = min(kMergeTile, la + lb - d0);
-  if (threadIdx.x < 2) {
-    const int diag = d0 + (threadIdx.x == 0 ? 0 : cnt);
-    int lo = max(0, diag - lb), hi = min(diag, la);
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (A[mid] < B[diag - 1 - mid])
-        lo = mid + 1;
-      else
-        hi = mid;
-    }
-    s_split[threadIdx.x] = lo;
+  // The merge-path splits of this CTA's first and one-past-last outputs:
+  // ans = #A elements among the first `diag` outputs, the first i in
+  // [lo, hi] with !(A[i] < B[diag-1-i]).  Each half of the CTA narrows one
+  // split by probing 128 evenly spaced candidates per round (a span of
+  // 2^15 resolves in 3 rounds instead of 15 dependent probes).
+  constexpr int kGroup = kMergeThreads / 2;
+  const int grp = threadIdx.x / kGroup, u = threadIdx.x % kGroup;
+  const int diag = d0 + (grp == 0 ? 0 : cnt);
+  if (u == 0) {
+    s_lo[grp] = max(0, diag - lb);
+    s_hi[grp] = min(diag, la);
   }
   __syncthreads();
-  const int ia0 = s_split[0], ia1 = s_split[1];
+  for (int round = 0; round < 8; ++round) {
+    const int lo = s_lo[grp], hi = s_hi[grp];
+    const bool active = s_hi[0] > s_lo[0] || s_hi[1] > s_lo[1];  // uniform
+    __syncthreads();
+    if (!active) break;
+    if (u == 0) s_cnt[grp] = 0;
+    __syncthreads();
+    const int span = hi - lo;
+    const int step = (span + kGroup - 1) / kGroup;
+    const int i = lo + u * step;
+    const bool t = span > 0 && i < hi && A[i] < B[diag - 1 - i];
+    const uint32_t bal = __ballot_sync(0xffffffffu, t);
+    if ((threadIdx.x & 31) == 0 && bal) atomicAdd(&s_cnt[grp], __popc(bal));
+    __syncthreads();
+    if (u == 0 && span > 0) {
+      const int c = s_cnt[grp];
+      s_lo[grp] = (c > 0) ? lo + (c - 1) * step + 1 : lo;
+      s_hi[grp] = min(hi, lo + c * step);
+    }
+    __syncthreads();
+  }
+  const int ia0 = s_lo[0], ia1 = s_lo[1];
   const int ib0 = d0 - ia0, ib1 = d0 + cnt - ia1;
   const int na = ia1 - ia0, nb = ib1 - ib0;  // na + nb == cnt
   for (int i = threadIdx.x; i < na; i += kMergeThreads) s_in[spad(i)] = A[ia0 + i];
