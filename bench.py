@@ -116,15 +116,15 @@ def launches_per_step(w):
     """Kernels the library launches per step (select + sparse attention) for
     sort mode QK: a norm pass, a chunk sort and ceil(log2(L / 4096)) merge
     passes (Q and K together in each), one statistics, one score and one
-    top-kappa kernel; then one row-gather kernel (Q, K, V) and the attention
-    kernel."""
+    top-kappa kernel; then the tile-pair list kernel, one row-gather kernel
+    (Q, K, V) and the attention kernel."""
     passes = 0
     width = 4096
     while width < w.seqlen:
         width *= 2
         passes += 1
     select = 2 + passes + 3
-    attn = 2
+    attn = 3
     return select + attn
 
 
@@ -402,7 +402,7 @@ def main():
         vs_baseline=None, dtype="bf16", data="synthetic", config=workload_config(w),
         roofline=dict(bound="tensor", achieved=round(att_tflops, 2), peak=pk["bf16"], unit="TFLOP/s",
                       frac=round(att_tflops / pk["bf16"], 4), traffic=attn_traffic(w.name),
-                      kernel="ba_sparse_attn (row gathers + tcgen05 attention kernel)",
+                      kernel="ba_sparse_attn (tile-pair lists + row gathers + tcgen05 attention kernel)",
                       peak_kind=f"bf16 dense burst, {pk['source']}",
                       algorithmic_flops_per_launch=attn_flops),
         e2e=dict(value=round(whole_job_tflops(world, flops_step, e2e_ms), 3), unit=UNIT,

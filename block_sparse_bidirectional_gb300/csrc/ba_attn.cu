@@ -109,6 +109,19 @@ struct AttnParams {
   const uint16_t *pair_lists;  // [b*h][npairs][2][N]: per tile, common blocks first
   const int32_t *pair_counts;  // [b*h][npairs][4]: n0, n1, common, -
   const int32_t *perm_q;  // sorted query position -> original row (nullable)
+  // Row gathers done inside the kernel by warps 2-3: CTA `pair` of head bh
+  // writes rows [pair * slice_rows, +slice_rows) of Q', K', V' of head
+  // bh + lookahead, then counts itself in ready[bh + lookahead].  CTAs of a
+  // head >= lookahead wait for ready[head] == npairs before their first TMA
+  // load; heads < lookahead were gathered by a kernel launched before.
+  // ready == nullptr: no in-kernel gathers, no waits.
+  const int32_t *perm_k;
+  const __nv_bfloat16 *src_q, *src_k, *src_v;  // unpermuted inputs
+  __nv_bfloat16 *dst_q, *dst_k, *dst_v;        // Q' (or null), K' and V' (or null)
+  int *ready;
+  int lookahead;
+  int bh_total;
+  int slice_rows;
   __nv_bfloat16 *o;
   float *lse;
   float scale_log2;       // scale * log2(e)
@@ -118,6 +131,42 @@ struct AttnParams {
 // the tile selected it.  Sparse tiles read their entries from the pair list
 // (k_pair_lists); dense tiles walk every block.
 __device__ __forceinline__ uint32_t dense_entry(int j) { return static_cast<uint32_t>(j) | (3u << 12); }
+
+// One CTA's share of the row gathers of head hp (64 threads, 16 bytes each
+// per access; kGatherUnroll rows per thread in flight).
+constexpr int kGatherUnroll = 4;
+
+template <int D>
+__device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pair, int tid) {
+  constexpr int VPR = D / 8;      // 16-byte pieces per row
+  constexpr int RPP = 64 / VPR;   // rows per pass of the 64 threads
+  const int c = tid % VPR, rsub = tid / VPR;
+  const int64_t base = static_cast<int64_t>(hp) * p.L;
+  const int r_begin = pair * p.slice_rows;
+  const int r_end = min(p.L, r_begin + p.slice_rows);
+  for (int op = 0; op < 3; ++op) {
+    const __nv_bfloat16 *src = op == 0 ? p.src_q : (op == 1 ? p.src_k : p.src_v);
+    __nv_bfloat16 *dst = op == 0 ? p.dst_q : (op == 1 ? p.dst_k : p.dst_v);
+    const int32_t *perm = op == 0 ? p.perm_q : p.perm_k;
+    if (dst == nullptr) continue;
+    for (int r0 = r_begin; r0 < r_end; r0 += RPP * kGatherUnroll) {
+      uint4 v[kGatherUnroll];
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int row = r0 + u * RPP + rsub;
+        if (row < r_end) {
+          const int64_t s = base + min(max(__ldg(perm + base + row), 0), p.L - 1);
+          v[u] = __ldg(reinterpret_cast<const uint4 *>(src + s * D) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kGatherUnroll; ++u) {
+        const int row = r0 + u * RPP + rsub;
+        if (row < r_end) reinterpret_cast<uint4 *>(dst + (base + row) * D)[c] = v[u];
+      }
+    }
+  }
+}
 
 template <int D, int BK, bool kDense>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -197,6 +246,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
+      // this head's Q', K', V' rows come from CTAs of an earlier head; on a
+      // timeout the error word is set and the loads go ahead regardless
+      if (p.ready != nullptr && bh >= p.lookahead)
+        wait_counter_at_least(p.ready + bh, p.npairs, kSiteRowsReady);
       uint32_t qbytes = 0;
       for (int t = 0; t < kTiles; ++t) qbytes += n_t[t] > 0 ? Lay::kQBytes : 0;
       mbar_arrive_expect_tx(q_full, qbytes);
@@ -306,6 +359,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
+    } else if (warp >= 2 && p.ready != nullptr) {
+      // ===================== row gathers for a later head ===================
+      const int hp = bh + p.lookahead;
+      if (hp < p.bh_total) {
+        gather_slice<D>(p, hp, pair, threadIdx.x - 64);
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+        if (threadIdx.x == 64) {
+          __threadfence();
+          atomicAdd(p.ready + hp, 1);
+        }
+      }
     }
   } else {
     reg_alloc<RegSplit<BK>::kHigh>();
@@ -329,17 +393,22 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     float lcorr = 0.f;
     bool ok = true;
     const int n = n_t[t];
+    // The softmax needs an entry only to mask: the other query block's
+    // entries (64-row blocks) or the ragged last key block.  With 128-row
+    // blocks every entry of a tile's list is its own, so when L is a multiple
+    // of 128 the list is never read here.
+    const bool read_list = !kDense && (BK < kTileM || p.L % BK != 0);
     uint32_t my_e = 0;  // sparse: 32 list entries at a time, one per lane
     for (int j = 0; j < n; ++j) {
       uint32_t e;
-      if (!kDense) {
+      if (read_list) {
         if ((j & 31) == 0) my_e = (j + lane < n) ? __ldg(plist[t] + j + lane) : 0u;
         e = __shfl_sync(0xffffffffu, my_e, j & 31);
       } else {
-        e = dense_entry(j);
+        e = kDense ? dense_entry(j) : 0u;  // sparse: block 0, never the ragged one
       }
       const int blk = e & 0xFFF;
-      const bool sel = (e >> (12 + my_g)) & 1u;
+      const bool sel = (BK == kTileM) || ((e >> (12 + my_g)) & 1u);
       const int valid_cols = min(BK, p.L - blk * BK);
       ok = mbar_wait(&s_full[t], j & 1, kSiteSFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -481,7 +550,7 @@ __global__ void __launch_bounds__(256) k_gather_rows(const GatherJobs jobs, int6
 #pragma unroll
   for (int u = 0; u < kGatherRows; ++u) {
     const int64_t row = row0 + u * RPW;
-    src[u] = (row < rows) ? (row / L) * L + __ldg(perm + row) : -1;
+    src[u] = (row < rows) ? (row / L) * L + min(max(__ldg(perm + row), 0), L - 1) : -1;
   }
   uint4 v[kGatherRows];
 #pragma unroll
@@ -507,9 +576,15 @@ constexpr int kPairWords = kMaxBlocks / 32;
 template <int G>
 __global__ void __launch_bounds__(kPairWarps * 32) k_pair_lists(
     const int32_t *__restrict__ idx, int N, int kappa, int n_tiles, int npairs, int64_t total,
-    uint16_t *__restrict__ lists, int32_t *__restrict__ counts) {
+    uint16_t *__restrict__ lists, int32_t *__restrict__ counts, int *__restrict__ ready,
+    int n_ready) {
   __shared__ uint32_t bm[kPairWarps][kTiles][G][kPairWords];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  {
+    // the attention kernel's per-head gather counters start from zero
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (ready != nullptr && i < n_ready) ready[i] = 0;
+  }
   const int64_t gp = static_cast<int64_t>(blockIdx.x) * kPairWarps + warp;
   if (gp >= total) return;  // warp-uniform; no block barrier below
   const int64_t bh = gp / npairs;
@@ -607,7 +682,24 @@ static size_t pair_list_bytes(int64_t bh, int L, int B) {
 
 size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool perm_k) {
   const size_t t = align256(static_cast<size_t>(bh) * L * D * 2);
-  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0) + pair_list_bytes(bh, L, B);
+  const size_t ready = (perm_q || perm_k) ? align256(static_cast<size_t>(bh) * sizeof(int)) : 0;
+  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0) + pair_list_bytes(bh, L, B) + ready;
+}
+
+// Heads between an attention CTA and the head whose rows it gathers: far
+// enough back in launch order (about two waves of CTAs) that a head's rows
+// are complete before its first CTA starts.
+static int gather_lookahead(int npairs) {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      sms = n;
+    else
+      sms = 152;
+  }
+  return (2 * sms + npairs - 1) / npairs;
 }
 
 template <int D, int BK, bool kDense>
@@ -666,28 +758,38 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   int32_t *pair_counts = nullptr;
   const int n_tiles = (L + kTileM - 1) / kTileM;
   const int npairs = (n_tiles + kTiles - 1) / kTiles;
+  // Gathers: the first `lookahead` heads by k_gather_rows before the
+  // attention kernel, the others by the attention CTAs of earlier heads.
+  int *ready = nullptr;
+  const int lookahead = gather_lookahead(npairs);
+  const bool in_kernel_gathers = !dense && njobs > 0 && lookahead < bh;
   if (!dense) {
     const int64_t nblk = (L + BK - 1) / BK;
     pair_lists = reinterpret_cast<uint16_t *>(ws);
-    pair_counts = reinterpret_cast<int32_t *>(
-        ws + align256(static_cast<size_t>(bh * npairs * kTiles * nblk) * sizeof(uint16_t)));
+    const size_t list_bytes = align256(static_cast<size_t>(bh * npairs * kTiles * nblk) * sizeof(uint16_t));
+    pair_counts = reinterpret_cast<int32_t *>(ws + list_bytes);
+    if (in_kernel_gathers) ready = reinterpret_cast<int *>(ws + pair_list_bytes(bh, L, BK));
     const int64_t total = bh * npairs;
     const unsigned grid = static_cast<unsigned>((total + kPairWarps - 1) / kPairWarps);
+    const int n_ready = ready ? static_cast<int>(bh) : 0;
     if (BK == 128)
       k_pair_lists<1><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
-                                                        n_tiles, npairs, total, pair_lists, pair_counts);
+                                                        n_tiles, npairs, total, pair_lists, pair_counts,
+                                                        ready, n_ready);
     else
       k_pair_lists<2><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
-                                                        n_tiles, npairs, total, pair_lists, pair_counts);
+                                                        n_tiles, npairs, total, pair_lists, pair_counts,
+                                                        ready, n_ready);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (njobs > 0) {
+    const int64_t grows = in_kernel_gathers ? static_cast<int64_t>(lookahead) * L : rows;
     const int rows_per_cta = (256 / (D / 8)) * kGatherRows;
-    const dim3 grid(static_cast<unsigned>((rows + rows_per_cta - 1) / rows_per_cta), njobs);
+    const dim3 grid(static_cast<unsigned>((grows + rows_per_cta - 1) / rows_per_cta), njobs);
     if (D == 128)
-      k_gather_rows<128><<<grid, 256, 0, st>>>(jobs, rows, L);
+      k_gather_rows<128><<<grid, 256, 0, st>>>(jobs, grows, L);
     else
-      k_gather_rows<64><<<grid, 256, 0, st>>>(jobs, rows, L);
+      k_gather_rows<64><<<grid, 256, 0, st>>>(jobs, grows, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   alignas(64) CUtensorMap mq, mk, mv;
@@ -703,6 +805,17 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   p.pair_lists = pair_lists;
   p.pair_counts = pair_counts;
   p.perm_q = a.perm_q;
+  p.perm_k = a.perm_k;
+  p.src_q = static_cast<const __nv_bfloat16 *>(a.q);
+  p.src_k = static_cast<const __nv_bfloat16 *>(a.k);
+  p.src_v = static_cast<const __nv_bfloat16 *>(a.v);
+  p.dst_q = a.perm_q ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(qs)) : nullptr;
+  p.dst_k = a.perm_k ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(ks)) : nullptr;
+  p.dst_v = a.perm_k ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(vs)) : nullptr;
+  p.ready = ready;
+  p.lookahead = lookahead;
+  p.bh_total = static_cast<int>(bh);
+  p.slice_rows = (L + npairs - 1) / npairs;
   p.o = static_cast<__nv_bfloat16 *>(a.o);
   p.lse = a.lse;
   const float scale = (a.scale > 0.f) ? a.scale : 1.0f / sqrtf(static_cast<float>(D));

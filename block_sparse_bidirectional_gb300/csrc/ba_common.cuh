@@ -31,6 +31,7 @@ enum WaitSite : uint32_t {
   kSitePFull = 7,
   kSiteODone = 8,
   kSiteDrain = 9,
+  kSiteRowsReady = 10,
 };
 
 // A wait gives up after this many nanoseconds of wall time (2 s).
@@ -131,6 +132,28 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+
+// Waits (bounded) until *counter >= target with acquire semantics at GPU
+// scope, then orders the data those writers published before this thread's
+// later TMA (async-proxy) reads of global memory.  On a timeout the site is
+// recorded and the wait returns false.
+__device__ __forceinline__ bool wait_counter_at_least(const int *counter, int target, uint32_t site) {
+  const uint64_t t0 = global_ns();
+  bool ok = true;
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) break;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      report_timeout(site);
+      ok = false;
+      break;
+    }
+    __nanosleep(200);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return ok;
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {

@@ -57,8 +57,10 @@ def test_workspace_sizes():
     # tile-pair lists (uint16, two tiles of N entries per CTA) and their counts
     npairs = ((L + 127) // 128 + 1) // 2
     pl = a256(b * h * npairs * 2 * N * 2) + a256(b * h * npairs * 4 * 4)
-    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t + pl
-    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t + pl
+    # with a permutation: the permuted copies and one gather counter per head
+    rc = a256(b * h * 4)
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t + pl + rc
+    assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t + pl + rc
     assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 0) == pl
     # unsupported shapes report 0
     assert lib.ba_select_workspace_size(1, 1, 1024, 96, 64, 8, 3, 0) == 0
