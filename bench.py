@@ -49,7 +49,7 @@ def peaks():
 # DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
 # of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
 # for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
-ATTN_TRAFFIC = {"ultra64k": dict(bytes=1722405376, kernel_sha="25daa684ca8dea8f")}
+ATTN_TRAFFIC = {"ultra64k": dict(bytes=5255004416, kernel_sha="61ccffa76cce4036")}
 
 
 def attn_traffic(workload: str):
@@ -305,9 +305,12 @@ def main():
     o = torch.empty_like(qd)
     lse = torch.empty((b, h, L), dtype=torch.float32, device=dev)
 
-    def step(qx, kx, vx):
+    def step_to(qx, kx, vx, ox, lx):
         bsb.ba_select_into(qx, kx, B, kappa, 1.0, 3, 0, perm_q, perm_k, idx, mask, None, ws_sel)
-        bsb.ba_sparse_attn_into(qx, kx, vx, B, perm_q, perm_k, idx, 0.0, o, lse, ws_att)
+        bsb.ba_sparse_attn_into(qx, kx, vx, B, perm_q, perm_k, idx, 0.0, ox, lx, ws_att)
+
+    def step(qx, kx, vx):
+        step_to(qx, kx, vx, o, lse)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
@@ -366,23 +369,80 @@ def main():
     dense_ms = e0.elapsed_time(e1) / args.dense_steps
     del od, lsed
 
+    # ---- isolated selection (SparseD §3.3) at the same shape ----------------
+    # the first quarter of the tokens as prompt, half of each part's key blocks
+    pre = (L // 4) // B * B
+    n_pre = pre // B
+    kpre, kgen = max(1, n_pre // 2), max(1, (N - n_pre) // 2)
+    idx_iso = torch.empty((b, h, N, kpre + kgen), **i32)
+    ws_iso = torch.empty(bsb.select_workspace_size(b, h, L, d, B, kpre + kgen, 3, 0),
+                         dtype=torch.uint8, device=dev)
+
+    def iso():
+        bsb.ba_select_isolated_into(qd, kd, B, pre, kpre, kgen, 1.0, 3, 0, perm_q, perm_k, idx_iso,
+                                    mask, None, ws_iso)
+    iso()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(5):
+        iso()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    iso_ms = e0.elapsed_time(e1) / 5
+    del idx_iso, ws_iso
+
     # ---- end to end through the public API from pinned host memory ----------
+    # Every step uploads its inputs (Q, K, V) from pinned host memory and
+    # downloads its result (O, LSE) inside the timed region.  Inputs and
+    # outputs are double-buffered and the copies run on a second stream, so
+    # step i+1's upload and step i's download overlap step i's compute; events
+    # order every reuse of a buffer.
+    e2e_steps = max(3, min(args.steps, 10))
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    qx, kx, vx = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    e2e_steps = max(3, min(args.steps, 5))
-    for _ in range(2):
-        qx.copy_(qh, non_blocking=True); kx.copy_(kh, non_blocking=True); vx.copy_(vh, non_blocking=True)
-        step(qx, kx, vx)
-        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    xin = [tuple(torch.empty_like(t) for t in (qd, kd, vd)) for _ in range(2)]
+    xout = [(torch.empty_like(o), torch.empty_like(lse)) for _ in range(2)]
+    hout = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+             torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for _ in range(2)]
+    cstream = torch.cuda.Stream(dev)
+
+    def e2e_run(n, start_event):
+        ev_in = [torch.cuda.Event() for _ in range(n)]    # step i's inputs on the device
+        ev_done = [torch.cuda.Event() for _ in range(n)]  # step i computed
+        ev_out = [torch.cuda.Event() for _ in range(n)]   # step i's result on the host
+        cstream.wait_event(start_event)
+
+        def upload(i):
+            with torch.cuda.stream(cstream):
+                if i >= 2:
+                    cstream.wait_event(ev_done[i - 2])    # this slot's inputs are consumed
+                for dst, src in zip(xin[i % 2], (qh, kh, vh)):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[i].record(cstream)
+
+        upload(0)
+        for i in range(n):
+            sl = i % 2
+            if i + 1 < n:
+                upload(i + 1)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])          # this slot's outputs are downloaded
+            step_to(*xin[sl], *xout[sl])
+            ev_done[i].record(stream)
+            with torch.cuda.stream(cstream):
+                cstream.wait_event(ev_done[i])
+                hout[sl][0].copy_(xout[sl][0], non_blocking=True)
+                hout[sl][1].copy_(xout[sl][1], non_blocking=True)
+                ev_out[i].record(cstream)
+        stream.wait_event(ev_out[n - 1])
+
+    w0 = torch.cuda.Event()
+    w0.record(stream)
+    e2e_run(2, w0)
     torch.cuda.synchronize(dev)
     barrier()
     e0.record(stream)
-    for _ in range(e2e_steps):
-        qx.copy_(qh, non_blocking=True); kx.copy_(kh, non_blocking=True); vx.copy_(vh, non_blocking=True)
-        step(qx, kx, vx)
-        oh.copy_(o, non_blocking=True); lh.copy_(lse, non_blocking=True)
+    e2e_run(e2e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
@@ -406,7 +466,8 @@ def main():
                       peak_kind=f"bf16 dense burst, {pk['source']}",
                       algorithmic_flops_per_launch=attn_flops),
         e2e=dict(value=round(whole_job_tflops(world, flops_step, e2e_ms), 3), unit=UNIT,
-                 ms_per_step=round(e2e_ms, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                 ms_per_step=round(e2e_ms, 3), h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                 steps=e2e_steps, copies="second stream, double-buffered, overlapping compute"),
         gpu_launches=launches_per_step(w) * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
                     samples=clk["samples"]),
@@ -422,6 +483,8 @@ def main():
             dense_tflops=round(flops_step / (dense_ms * 1e-3) / 1e12, 2),
             dense_frac_tensor_burst=round(flops_step / (dense_ms * 1e-3) / 1e12 / pk["bf16"], 4),
             speedup_vs_dense=round(dense_ms / ms_step, 3),
+            isolated_select_ms=round(iso_ms, 4),
+            isolated_select=f"prefill {pre} tokens, kappa {kpre} + {kgen}, sort QK",
             density=round(attn_flops / flops_step, 4)),
     )
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

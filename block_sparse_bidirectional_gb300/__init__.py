@@ -19,7 +19,8 @@ import re
 
 from . import _build
 
-__all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_sparse_attn", "ba_sparse_attn_into",
+__all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_select_isolated",
+           "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into",
            "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
            "last_device_error", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
@@ -44,6 +45,8 @@ _SIGS = {
     "ba_attn_dense": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [_c_float] + [_c_void_p] * 3),
     "ba_last_device_error": (_c_int, [_c_void_p, _c_u32p]),
     "ba_merge_lse": (_c_int, [_c_void_p] * 4 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
+    "ba_select_isolated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 8 + [_c_float, _c_int, _c_int]
+                           + [_c_void_p] * 6 + [_c_size, _c_void_p]),
     "ba_select_noalloc": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int]
                           + [_c_void_p] * 5 + [_c_void_p]),
 }
@@ -135,6 +138,49 @@ def ba_select_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, per
                        _ptr(perm_q), _ptr(perm_k), _ptr(block_idx), _ptr(block_mask),
                        _ptr(block_scores), _ptr(workspace), ws_bytes, _stream(q.device))
     _check(st, "ba_select")
+
+
+def ba_select_isolated_into(q, k, block, prefill_len, kappa_prefill, kappa_generation, beta, sort_mode,
+                            sort_window, perm_q, perm_k, block_idx, block_mask, block_scores, workspace):
+    """ba_select_isolated writing caller-allocated tensors (no allocation)."""
+    lib = load()
+    _need_cuda(q, k, perm_q, perm_k, block_idx, block_mask, block_scores, workspace)
+    b, h, L, d = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib.ba_select_isolated(_ptr(q), _ptr(k), b, h, L, d, block, prefill_len, kappa_prefill,
+                                kappa_generation, float(beta), sort_mode, sort_window, _ptr(perm_q),
+                                _ptr(perm_k), _ptr(block_idx), _ptr(block_mask), _ptr(block_scores),
+                                _ptr(workspace), ws_bytes, _stream(q.device))
+    _check(st, "ba_select_isolated")
+
+
+def ba_select_isolated(q, k, block, prefill_len, kappa_prefill, kappa_generation, beta=1.0,
+                       sort_mode=SORT_QK, sort_window=0, return_scores=False, workspace=None):
+    """Isolated selection (SparseD §3.3 Eq. 5-6 over BA-Att's block scores):
+    per query block, kappa_prefill key blocks from [0, prefill_len) and
+    kappa_generation from [prefill_len, L).  Returns the same dict as
+    ba_select, block_idx holding kappa_prefill + kappa_generation ids."""
+    torch = _torch()
+    _need_cuda(q, k)
+    b, h, L, d = q.shape
+    N = -(-L // block)
+    kappa = kappa_prefill + kappa_generation
+    dev = q.device
+    out = dict(
+        perm_q=torch.empty((b, h, L), dtype=torch.int32, device=dev),
+        perm_k=torch.empty((b, h, L), dtype=torch.int32, device=dev),
+        block_idx=torch.empty((b, h, N, kappa), dtype=torch.int32, device=dev),
+        block_mask=torch.empty((b, h, N, -(-N // 32)), dtype=torch.int32, device=dev),
+        block_scores=torch.empty((b, h, N, N), dtype=torch.float32, device=dev) if return_scores else None,
+    )
+    if workspace is None:
+        workspace = _workspace(select_workspace_size(b, h, L, d, block, kappa, sort_mode, sort_window), dev)
+    ba_select_isolated_into(q, k, block, prefill_len, kappa_prefill, kappa_generation, beta, sort_mode,
+                            sort_window, out["perm_q"], out["perm_k"], out["block_idx"], out["block_mask"],
+                            out["block_scores"], workspace)
+    if not return_scores:
+        del out["block_scores"]
+    return out
 
 
 def ba_select_noalloc_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, perm_k,

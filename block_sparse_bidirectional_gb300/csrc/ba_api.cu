@@ -141,6 +141,57 @@ int ba_select(const void *q, const void *k, int batch, int heads, int seqlen, in
   return map_cuda(run_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ba_select_isolated(const void *q, const void *k, int batch, int heads, int seqlen,
+                       int head_dim, int block, int prefill_len, int kappa_prefill,
+                       int kappa_generation, float beta, int sort_mode, int sort_window,
+                       int32_t *perm_q, int32_t *perm_k, int32_t *block_idx,
+                       uint32_t *block_mask, float *block_scores, void *workspace,
+                       size_t workspace_bytes, ba_stream_t stream) {
+  int st = check_shape(batch, heads, seqlen, head_dim, block);
+  if (st != BA_OK) return st;
+  const int n = (seqlen + block - 1) / block;
+  if (prefill_len <= 0 || prefill_len >= seqlen || prefill_len % block != 0)
+    return BA_ERR_INVALID_ARG;
+  const int n_pre = prefill_len / block, n_gen = n - n_pre;
+  if (kappa_prefill < 1 || kappa_prefill > n_pre) return BA_ERR_INVALID_ARG;
+  if (kappa_generation < 1 || kappa_generation > n_gen) return BA_ERR_INVALID_ARG;
+  const int kappa = kappa_prefill + kappa_generation;
+  if (!isfinite(beta)) return BA_ERR_INVALID_ARG;
+  if (sort_mode < 0 || sort_mode > 3) return BA_ERR_INVALID_ARG;
+  if (sort_window < 0 || (sort_window > 0 && sort_window % block != 0)) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !perm_q || !perm_k || !block_idx || !block_mask) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(perm_q) || !aligned16(perm_k) ||
+      !aligned16(block_idx) || !aligned16(block_mask) ||
+      (block_scores && !aligned16(block_scores)))
+    return BA_ERR_INVALID_ARG;
+  const size_t need = ba_select_workspace_size(batch, heads, seqlen, head_dim, block, kappa,
+                                               sort_mode, sort_window);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need ||
+                   (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+    return BA_ERR_WORKSPACE;
+  SelectArgs a;
+  a.q = q;
+  a.k = k;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.kappa = kappa;
+  a.beta = beta;
+  a.sort_mode = sort_mode;
+  a.sort_window = sort_window;
+  a.perm_q = perm_q;
+  a.perm_k = perm_k;
+  a.block_idx = block_idx;
+  a.block_mask = block_mask;
+  a.block_scores = block_scores;
+  a.workspace = workspace;
+  a.prefill_len = prefill_len;
+  a.kappa_prefill = kappa_prefill;
+  return map_cuda(run_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t ba_sparse_attn_workspace_size(int batch, int heads, int seqlen, int head_dim, int block,
                                      int kappa, int has_perm_q, int has_perm_k) {
   (void)kappa;

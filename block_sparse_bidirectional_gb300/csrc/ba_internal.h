@@ -16,6 +16,11 @@ struct SelectArgs {
   uint32_t *block_mask;
   float *block_scores;
   void *workspace;
+  // isolated selection (SparseD §3.3): > 0 splits the keys at this token
+  // (a multiple of block); kappa_prefill of the kappa blocks per row come
+  // from the first prefill_len / block key blocks
+  int prefill_len = 0;
+  int kappa_prefill = 0;
 };
 
 struct AttnArgs {

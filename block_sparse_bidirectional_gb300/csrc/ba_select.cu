@@ -95,12 +95,19 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
 // ---------------------------------------------------------------------------
 struct SortGeom {
   int L;        // tokens per sequence
-  int win;      // window length (== L for a whole-sequence sort)
+  int win;      // window length (== L for a whole-sequence sort); with a
+                // split, the longer of the two windows
   int nwin;     // windows per sequence
   int bh;       // sequences per tensor
+  int split;    // > 0: two windows, [0, split) and [split, L)
 };
 
+__device__ __forceinline__ int window_start(const SortGeom &g, int w) {
+  return g.split > 0 ? (w == 0 ? 0 : g.split) : w * g.win;
+}
+
 __device__ __forceinline__ int window_len(const SortGeom &g, int w) {
+  if (g.split > 0) return w == 0 ? g.split : g.L - g.split;
   const int start = w * g.win;
   return min(g.win, g.L - start);
 }
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
   const int c0 = blockIdx.x * kChunk;
   if (c0 >= wlen) return;  // uniform over the CTA
   const int n = min(kChunk, wlen - c0);
-  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win + c0;
+  const int64_t base = static_cast<int64_t>(seq) * g.L + window_start(g, w) + c0;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   // ---- warp-level bitonic sort of 256 keys; element e = i * 32 + lane ----
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
     dst = t;
   }
   int32_t *perm = (seq < g.bh) ? perm0 : perm1;
-  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + static_cast<int64_t>(w) * g.win + c0;
+  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w) + c0;
   for (int i = threadIdx.x; i < n; i += kSortThreads) {
     if (final_pass)
       perm[pbase + i] = static_cast<int32_t>(src[spad(i)] & 0xffffffffu);
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
   const int wlen = window_len(g, w);
   const int o_cta = blockIdx.x * kMergeTile;
   if (o_cta >= wlen) return;  // uniform over the CTA
-  const int64_t base = static_cast<int64_t>(seq) * g.L + static_cast<int64_t>(w) * g.win;
+  const int64_t base = static_cast<int64_t>(seq) * g.L + window_start(g, w);
   const int p0 = (o_cta / (2 * width)) * 2 * width;
   const int a1 = min(p0 + width, wlen), b1 = min(p0 + 2 * width, wlen);
   const int la = a1 - p0, lb = b1 - a1;
@@ -314,7 +321,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
     merge_path_8_smem(s_in, 0, na, na, nb, t0, min(kMergeItems, cnt - t0), s_out, t0);
   __syncthreads();
   int32_t *perm = (seq < g.bh) ? perm0 : perm1;
-  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + static_cast<int64_t>(w) * g.win;
+  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w);
   for (int i = threadIdx.x; i < cnt; i += kMergeThreads) {
     if (final_pass)
       perm[pbase + o_cta + i] = static_cast<int32_t>(s_out[spad(i)] & 0xffffffffu);
@@ -522,9 +529,38 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Keys of one row live in registers (KPL per lane, element e = i * 32 + lane).
+// The row is split in two parts, elements [0, n_first) with budget
+// kappa_first and [n_first, N) with budget kappa - kappa_first (isolated
+// prefill / generation selection); n_first == N is the plain top-kappa.
+template <int KPL>
+__device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int lane, int lo, int hi,
+                                               int k, uint32_t &T, int &need) {
+  T = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int e = i * 32 + lane;
+      cnt += (e >= lo && e < hi) && keys[i] >= cand;
+    }
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (cnt >= static_cast<uint32_t>(k)) T = cand;
+  }
+  uint32_t gt = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = i * 32 + lane;
+    gt += (e >= lo && e < hi) && keys[i] > T;
+  }
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  need = k - static_cast<int>(gt);  // >= 1 keys equal to T to take, lowest index first
+}
+
 template <int KPL>
 __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(const float *__restrict__ scores,
                                                           int64_t rows, int N, int kappa,
+                                                          int n_first, int kappa_first,
                                                           int32_t *__restrict__ idx,
                                                           uint32_t *__restrict__ mask) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -537,34 +573,34 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(const float *__restric
     const int e = i * 32 + lane;
     keys[i] = (e < N) ? order_key(src[e]) : 0u;  // 0 sorts below every real key
   }
-  uint32_t T = 0;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    uint32_t cnt = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) cnt += (i * 32 + lane < N) && keys[i] >= cand;
-    cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if (cnt >= static_cast<uint32_t>(kappa)) T = cand;
-  }
-  uint32_t gt = 0;
-#pragma unroll
-  for (int i = 0; i < KPL; ++i) gt += (i * 32 + lane < N) && keys[i] > T;
-  gt = __reduce_add_sync(0xffffffffu, gt);
-  const int need = kappa - static_cast<int>(gt);  // >= 1 equal keys to take
+  uint32_t T0, T1 = 0;
+  int need0, need1 = 0;
+  part_threshold<KPL>(keys, lane, 0, n_first, kappa_first, T0, need0);
+  const bool two = n_first < N;
+  if (two) part_threshold<KPL>(keys, lane, n_first, N, kappa - kappa_first, T1, need1);
   const int nwords = (N + 31) / 32;
   const uint32_t lt_mask = (1u << lane) - 1u;
-  int taken = 0, base = 0;
+  int taken0 = 0, taken1 = 0, base = 0;
 #pragma unroll
   for (int wd = 0; wd < KPL; ++wd) {
     if (wd >= nwords) break;
     const int e = wd * 32 + lane;
-    const bool valid = e < N;
+    const bool in0 = e < n_first, in1 = two && e >= n_first && e < N;
     const uint32_t key = keys[wd];
-    const uint32_t eqb = __ballot_sync(0xffffffffu, valid && key == T);
-    const int rem = need - taken;
-    const bool sel_eq = valid && key == T && __popc(eqb & lt_mask) < rem;
-    taken += min(__popc(eqb), max(rem, 0));
-    const uint32_t selb = __ballot_sync(0xffffffffu, (valid && key > T) || sel_eq);
+    const bool eq0 = in0 && key == T0, eq1 = in1 && key == T1;
+    const uint32_t eqb0 = __ballot_sync(0xffffffffu, eq0);
+    const int rem0 = need0 - taken0;
+    const bool sel_eq0 = eq0 && __popc(eqb0 & lt_mask) < rem0;
+    taken0 += min(__popc(eqb0), max(rem0, 0));
+    bool sel_eq1 = false;
+    if (two) {
+      const uint32_t eqb1 = __ballot_sync(0xffffffffu, eq1);
+      const int rem1 = need1 - taken1;
+      sel_eq1 = eq1 && __popc(eqb1 & lt_mask) < rem1;
+      taken1 += min(__popc(eqb1), max(rem1, 0));
+    }
+    const uint32_t selb = __ballot_sync(
+        0xffffffffu, (in0 && key > T0) || sel_eq0 || (in1 && key > T1) || sel_eq1);
     if (lane == 0) mask[row * nwords + wd] = selb;
     if ((selb >> lane) & 1u) idx[row * kappa + base + __popc(selb & lt_mask)] = e;
     base += __popc(selb);
@@ -604,12 +640,18 @@ size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode) {
 // perm0 (the first `bh` sequences) and perm1 (the rest).
 static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t *buf1,
                                   int32_t *perm0, int32_t *perm1, int nseq, int64_t bh, int L,
-                                  int win, cudaStream_t st) {
+                                  int win, int split, cudaStream_t st) {
   SortGeom g;
   g.L = L;
-  g.win = (win <= 0 || win >= L) ? L : win;
-  g.nwin = (L + g.win - 1) / g.win;
   g.bh = static_cast<int>(bh);
+  g.split = (split > 0 && split < L) ? split : 0;
+  if (g.split > 0) {
+    g.win = max(g.split, L - g.split);
+    g.nwin = 2;
+  } else {
+    g.win = (win <= 0 || win >= L) ? L : win;
+    g.nwin = (L + g.win - 1) / g.win;
+  }
   int npasses = 0;
   for (int w = kChunk; w < g.win; w <<= 1) ++npasses;
   const int chunks = (g.win + kChunk - 1) / kChunk;
@@ -709,10 +751,24 @@ cudaError_t run_select(const SelectArgs &a, cudaStream_t st) {
       k_sqnorm_keys<64><<<grid, 256, 0, st>>>(x0, x1, keys0, rows, L);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the chunk sort reads keys0 and writes keys1; merges ping-pong keys1 <-> keys0
-    if ((e = sort_sequences(keys0, keys1, keys0, perms[0], perms[nsorted - 1],
-                            static_cast<int>(nsorted * bh), bh, L, a.sort_window, st)) !=
-        cudaSuccess)
-      return e;
+    if (a.prefill_len == 0 || !sort_k) {
+      if ((e = sort_sequences(keys0, keys1, keys0, perms[0], perms[nsorted - 1],
+                              static_cast<int>(nsorted * bh), bh, L, a.sort_window, 0, st)) !=
+          cudaSuccess)
+        return e;
+    } else {
+      // isolated selection: keys are sorted inside [0, prefill) and
+      // [prefill, L) so no sorted key block mixes the two ranges; queries
+      // keep the caller's window
+      const int64_t qoff = sort_q ? rows : 0;  // K's keys follow Q's
+      if (sort_q && (e = sort_sequences(keys0, keys1, keys0, a.perm_q, a.perm_q,
+                                        static_cast<int>(bh), bh, L, a.sort_window, 0, st)) !=
+                        cudaSuccess)
+        return e;
+      if ((e = sort_sequences(keys0 + qoff, keys1 + qoff, keys0 + qoff, a.perm_k, a.perm_k,
+                              static_cast<int>(bh), bh, L, 0, a.prefill_len, st)) != cudaSuccess)
+        return e;
+    }
   }
 
   // steps 3-4: statistics on the (possibly) permuted blocks, Q and K together
@@ -732,14 +788,21 @@ cudaError_t run_select(const SelectArgs &a, cudaStream_t st) {
   // steps 8-11: top-kappa (keys of a row in registers: 32 * KPL >= N)
   const int64_t qrows = bh * N;
   const unsigned tgrid = static_cast<unsigned>((qrows + kTopkWarps - 1) / kTopkWarps);
+  // isolated selection: the first prefill_len / B key blocks are the prefill part
+  const int n_first = a.prefill_len > 0 ? a.prefill_len / B : N;
+  const int k_first = a.prefill_len > 0 ? a.kappa_prefill : a.kappa;
   if (N <= 256)
-    k_topk<8><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+    k_topk<8><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, n_first, k_first,
+                                                 a.block_idx, a.block_mask);
   else if (N <= 512)
-    k_topk<16><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+    k_topk<16><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, n_first, k_first,
+                                                  a.block_idx, a.block_mask);
   else if (N <= 1024)
-    k_topk<32><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+    k_topk<32><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, n_first, k_first,
+                                                  a.block_idx, a.block_mask);
   else
-    k_topk<128><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, a.block_idx, a.block_mask);
+    k_topk<128><<<tgrid, kTopkWarps * 32, 0, st>>>(scores, qrows, N, a.kappa, n_first, k_first,
+                                                   a.block_idx, a.block_mask);
   return cudaGetLastError();
 }
 

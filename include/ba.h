@@ -144,6 +144,37 @@ int ba_select_noalloc(const void *q, const void *k, int batch, int heads,
                       ba_stream_t stream);
 
 /*
+ * Isolated selection: ba_select with the key dimension split into a prefill
+ * range [0, prefill_len) and a generation range [prefill_len, L), each with
+ * its own budget, after SparseD §3.3 "Isolated Selection" (Eq. 5-6): every
+ * query block keeps its kappa_prefill best key blocks among the prefill
+ * blocks and its kappa_generation best among the generation blocks, so
+ * generation tokens, whose scores are low in early denoising steps, are not
+ * crowded out by prefill tokens.  Scores are BA-Att's (as in ba_select).
+ * With a key sort (sort_mode 1 or 3) the keys are norm-sorted inside each
+ * range separately, so no sorted key block mixes the two; queries are sorted
+ * as in ba_select (sort_window applies to them only).
+ *
+ * prefill_len      tokens of the prefill part: a multiple of block with
+ *                  0 < prefill_len < L, else BA_ERR_INVALID_ARG.
+ * kappa_prefill    1 <= kappa_prefill <= prefill_len / block.
+ * kappa_generation 1 <= kappa_generation <= N - prefill_len / block.
+ * block_idx        int32 [b,h,N,kappa_prefill + kappa_generation], ascending
+ *                  (prefill blocks first, as their ids are lower).
+ * Other arguments, outputs, workspace (ba_select_workspace_size with kappa =
+ * kappa_prefill + kappa_generation) and errors as in ba_select.  The result
+ * feeds ba_sparse_attn with kappa = kappa_prefill + kappa_generation.
+ */
+int ba_select_isolated(const void *q, const void *k, int batch, int heads,
+                       int seqlen, int head_dim, int block, int prefill_len,
+                       int kappa_prefill, int kappa_generation, float beta,
+                       int sort_mode, int sort_window, int32_t *perm_q,
+                       int32_t *perm_k, int32_t *block_idx,
+                       uint32_t *block_mask, float *block_scores,
+                       void *workspace, size_t workspace_bytes,
+                       ba_stream_t stream);
+
+/*
  * Block-sparse attention: BA-Att paper Algorithm 1 step 12 (§2 block-sparse
  * attention; the masked softmax of SparseD §3.1 Eq. 3-4).  For the token at
  * sorted query position r (query block g = r / B):

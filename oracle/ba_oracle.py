@@ -13,6 +13,8 @@ Sources (cited by page title and section/equation):
   Algorithm 1.
 * "SparseD: Sparse Attention for Diffusion Language Models", §3.1 Eq. 3-4
   (the 0 / -inf sparse mask added to the logits before the softmax).
+* "SparseD: Sparse Attention for Diffusion Language Models", §3.3 "Isolated
+  Selection", Eq. 5-6: prefill and generation keys are selected separately.
 * The LoSA summary post ("merge and update" step): prefix and suffix attention
   results are combined through their log-normaliser (online softmax).
 
@@ -222,6 +224,87 @@ def ba_select(Q, K, B, kappa, beta=1.0, sort_mode=SORT_QK, window=0,
             r = select_one(Q[bi, hi], K[bi, hi], B, kappa, beta, sort_mode, window,
                            None if perm_q is None else perm_q[bi, hi],
                            None if perm_k is None else perm_k[bi, hi])
+            for key in out:
+                out[key][bi, hi] = r[key]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Isolated selection (SparseD §3.3 "Isolated Selection", Eq. 5-6) over the
+# BA-Att block scores
+# ---------------------------------------------------------------------------
+#
+# SparseD splits the key dimension into prefill tokens [0, p) and generation
+# tokens [p, L) and keeps the top share of each range on its own (Eq. 6), the
+# selected set being the union of the two (Eq. 5).  Applied to BA-Att's block
+# scores: p is a multiple of B, the key norm sort runs inside each range (so
+# a sorted key block never mixes the two), and each query-block row keeps its
+# kappa_pre best prefill blocks and its kappa_gen best generation blocks.
+
+def split_sort_permutation(s: np.ndarray, split: int) -> np.ndarray:
+    """Eq. 10's stable non-decreasing sort, run separately on [0, split) and
+    [split, L): positions below ``split`` hold prefill tokens only."""
+    L = s.shape[0]
+    out = np.empty(L, dtype=np.int64)
+    out[:split] = np.argsort(s[:split], kind="stable")
+    out[split:] = split + np.argsort(s[split:], kind="stable")
+    return out
+
+
+def topk_blocks_isolated(scores: np.ndarray, n_pre: int, kappa_pre: int, kappa_gen: int):
+    """Eq. 5-6: per row, the top ``kappa_pre`` of the first ``n_pre`` key
+    blocks united with the top ``kappa_gen`` of the rest (ties to the lower
+    index within each part).  Returns (idx [Nq, kappa_pre + kappa_gen]
+    ascending, mask [Nq, Nk] bool)."""
+    nq, nk = scores.shape
+    idx_pre, _ = topk_blocks(scores[:, :n_pre], kappa_pre)
+    idx_gen, _ = topk_blocks(scores[:, n_pre:], kappa_gen)
+    idx = np.concatenate([idx_pre, idx_gen + n_pre], axis=1)
+    mask = np.zeros((nq, nk), dtype=bool)
+    np.put_along_axis(mask, idx, True, axis=-1)
+    return idx, mask
+
+
+def select_isolated_one(q, k, B, prefill_len, kappa_pre, kappa_gen, beta=1.0,
+                        sort_mode=SORT_QK, window=0, perm_q=None, perm_k=None):
+    """Isolated selection for one sequence (q, k [L, d] float64).  Queries
+    are sorted as in ``select_one`` (``window`` applies to them); keys inside
+    each of the two ranges.  ``perm_q`` / ``perm_k`` override the sorts."""
+    L = q.shape[0]
+    if prefill_len % B != 0 or not 0 < prefill_len < L:
+        raise ValueError("prefill_len must be a multiple of B inside (0, L)")
+    if perm_q is None:
+        perm_q = (norm_sort_permutation(token_norms(q), window)
+                  if sort_mode in (SORT_Q, SORT_QK) else identity_permutation(L))
+    if perm_k is None:
+        perm_k = (split_sort_permutation(token_norms(k), prefill_len)
+                  if sort_mode in (SORT_K, SORT_QK) else identity_permutation(L))
+    perm_q = np.asarray(perm_q, dtype=np.int64)
+    perm_k = np.asarray(perm_k, dtype=np.int64)
+    qbar, varq = block_moments(q[perm_q], B)
+    kbar, vark = block_moments(k[perm_k], B)
+    scores = compensated_logits(qbar, varq, kbar, vark, beta)
+    idx, mask = topk_blocks_isolated(scores, prefill_len // B, kappa_pre, kappa_gen)
+    return dict(perm_q=perm_q, perm_k=perm_k, qbar=qbar, varq=varq, kbar=kbar,
+                vark=vark, scores=scores, idx=idx, mask=mask)
+
+
+def ba_select_isolated(Q, K, B, prefill_len, kappa_pre, kappa_gen, beta=1.0,
+                       sort_mode=SORT_QK, window=0, perm_q=None, perm_k=None):
+    """Batched isolated selection, outputs shaped as in ``ba_select`` with
+    kappa = kappa_pre + kappa_gen."""
+    b, h, L, d = Q.shape
+    N = num_blocks(L, B)
+    kappa = kappa_pre + kappa_gen
+    out = dict(perm_q=np.empty((b, h, L), np.int64), perm_k=np.empty((b, h, L), np.int64),
+               idx=np.empty((b, h, N, kappa), np.int64), mask=np.empty((b, h, N, N), bool),
+               scores=np.empty((b, h, N, N)))
+    for bi in range(b):
+        for hi in range(h):
+            r = select_isolated_one(Q[bi, hi], K[bi, hi], B, prefill_len, kappa_pre, kappa_gen,
+                                    beta, sort_mode, window,
+                                    None if perm_q is None else perm_q[bi, hi],
+                                    None if perm_k is None else perm_k[bi, hi])
             for key in out:
                 out[key][bi, hi] = r[key]
     return out

@@ -98,6 +98,35 @@ def test_select_rejects(kw, status):
     assert _select(bsb.load(), **kw) == status
 
 
+def _select_iso(lib, **kw):
+    a = dict(q=P, k=P, b=1, h=1, L=1024, d=64, B=64, pre=256, kpre=2, kgen=6, beta=1.0, mode=3,
+             win=0, pq=P2, pk=P2, idx=P2, mask=P2, scores=None, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ba_select_isolated(a["q"], a["k"], a["b"], a["h"], a["L"], a["d"], a["B"], a["pre"],
+                                  a["kpre"], a["kgen"], a["beta"], a["mode"], a["win"], a["pq"],
+                                  a["pk"], a["idx"], a["mask"], a["scores"], a["ws"], a["ws_bytes"],
+                                  a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(pre=0), INVALID),             # no prefill part
+    (dict(pre=1024), INVALID),          # no generation part
+    (dict(pre=100), INVALID),           # not a multiple of the block
+    (dict(kpre=0), INVALID),
+    (dict(kpre=5), INVALID),            # more than the 4 prefill blocks
+    (dict(kgen=0), INVALID),
+    (dict(kgen=13), INVALID),           # more than the 12 generation blocks
+    (dict(q=None), INVALID),
+    (dict(mask=MIS), INVALID),
+    (dict(mode=4), INVALID),
+    (dict(win=100), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(ws_bytes=1024), WORKSPACE),
+])
+def test_select_isolated_rejects(kw, status):
+    assert _select_iso(bsb.load(), **kw) == status
+
+
 def _attn(lib, **kw):
     a = dict(q=P, k=P, v=P, b=1, h=1, L=1024, d=64, B=64, pq=P2, pk=P2, idx=P2, kappa=8, scale=0.0,
              o=P, lse=P, ws=P, ws_bytes=1 << 30, stream=None)

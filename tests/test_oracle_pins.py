@@ -273,11 +273,69 @@ def check_block_mass():
     np.testing.assert_allclose(A, ref, atol=1e-12)
 
 
+def check_isolated_sort():
+    """The split sort is Eq. 10 inside each range: with the split in the
+    middle it equals the windowed sort (window = L/2); for any split each
+    range holds its own tokens, non-decreasing, equal norms by lower index
+    (brute force over positions)."""
+    rng = _rng(31)
+    L = 24
+    s = rng.integers(0, 5, L).astype(float)       # many equal norms
+    np.testing.assert_array_equal(O.split_sort_permutation(s, L // 2),
+                                  O.norm_sort_permutation(s, window=L // 2))
+    for split in (4, 10, 20):
+        p = O.split_sort_permutation(s, split)
+        for lo, hi in ((0, split), (split, L)):
+            seg = p[lo:hi]
+            assert sorted(seg.tolist()) == list(range(lo, hi))
+            for a, b in zip(seg[:-1], seg[1:]):
+                assert s[a] < s[b] or (s[a] == s[b] and a < b)
+
+
+def check_isolated_topk_bruteforce():
+    """Eq. 5-6: each part's chosen set is, among all sets of its size inside
+    its own key range, the one with the largest score sum, equal sums going
+    to the lexicographically smallest index set (= ties to the lower index).
+    Integer scores make the sums exact and create ties."""
+    from itertools import combinations
+    rng = _rng(32)
+    nq, nk, n_pre = 5, 8, 3
+    scores = rng.integers(-3, 4, (nq, nk)).astype(float)
+    for kpre, kgen in ((1, 1), (2, 3), (3, 5)):
+        idx, mask = O.topk_blocks_isolated(scores, n_pre, kpre, kgen)
+        for r in range(nq):
+            want = []
+            for lo, hi, kk in ((0, n_pre, kpre), (n_pre, nk, kgen)):
+                best = min(combinations(range(lo, hi), kk),
+                           key=lambda c: (-sum(scores[r, j] for j in c), c))
+                want += list(best)
+            assert idx[r].tolist() == want
+            assert mask[r].tolist() == [j in want for j in range(nk)]
+
+
+def check_isolated_keeps_generation_block():
+    """SparseD's motivation for isolating (§3.3): when prefill keys dominate
+    the scores, a plain top-kappa spends the whole budget on prefill blocks,
+    while the isolated selection still keeps the best generation block."""
+    B, d = 4, 4
+    e = np.eye(d)
+    q = np.tile(e[0], (16, 1))                        # 4 query blocks along e0
+    k = np.concatenate([np.tile(3 * e[0], (8, 1)),    # prefill blocks 0-1: strong
+                        np.tile(-1 * e[0], (4, 1)),   # generation block 2: negative
+                        np.tile(1 * e[0], (4, 1))])   # generation block 3: weak but best
+    plain = O.select_one(q, k, B, 2, 0.0, O.SORT_NONE)
+    assert plain["idx"].tolist() == [[0, 1]] * 4
+    iso = O.select_isolated_one(q, k, B, 8, 1, 1, 0.0, O.SORT_NONE)
+    assert iso["idx"].tolist() == [[0, 3]] * 4
+
+
 ALL_CHECKS = [check_hand_example, check_sort_bruteforce, check_block_logit_bilinearity,
               check_compensation_identity, check_deviation_bound, check_topk_bruteforce,
               check_topk_equals_softmax_order, check_all_blocks_is_dense_attention,
               check_constant_v, check_masked_softmax_bruteforce, check_lse_merge,
-              check_ragged_tail_moments, check_kappa_rule, check_block_mass]
+              check_ragged_tail_moments, check_kappa_rule, check_block_mass,
+              check_isolated_sort, check_isolated_topk_bruteforce,
+              check_isolated_keeps_generation_block]
 
 
 @pytest.mark.parametrize("check", ALL_CHECKS, ids=lambda c: c.__name__)
@@ -375,8 +433,27 @@ def _attn_lse_no_max(q, k, v, perm_q, perm_k, idx, B, scale=None, query_blocks=N
     return out, lse - 1e-3
 
 
+def _split_sort_whole(s, split):
+    return _ORIG["norm_sort_permutation"](s, 0)
+
+
+def _isolated_no_offset(scores, n_pre, kappa_pre, kappa_gen):
+    nq, nk = scores.shape
+    idx_pre, _ = O.topk_blocks(scores[:, :n_pre], kappa_pre)
+    idx_gen, _ = O.topk_blocks(scores[:, n_pre:], kappa_gen)
+    idx = np.concatenate([idx_pre, idx_gen], axis=1)
+    mask = np.zeros((nq, nk), bool)
+    np.put_along_axis(mask, np.clip(idx, 0, nk - 1), True, axis=-1)
+    return idx, mask
+
+
+def _isolated_joint(scores, n_pre, kappa_pre, kappa_gen):
+    return O.topk_blocks(scores, kappa_pre + kappa_gen)
+
+
 _ORIG = {n: getattr(O, n) for n in ("block_moments", "covariance_compensation", "block_logits",
-                                      "topk_blocks", "norm_sort_permutation", "sparse_attention_one")}
+                                      "topk_blocks", "norm_sort_permutation", "sparse_attention_one",
+                                      "split_sort_permutation", "topk_blocks_isolated")}
 
 MUTANTS = [
     ("block_moments", _moments_sample_var),
@@ -389,6 +466,9 @@ MUTANTS = [
     ("norm_sort_permutation", _sort_unstable),
     ("sparse_attention_one", _attn_rows_unpermuted),
     ("sparse_attention_one", _attn_lse_no_max),
+    ("split_sort_permutation", _split_sort_whole),
+    ("topk_blocks_isolated", _isolated_no_offset),
+    ("topk_blocks_isolated", _isolated_joint),
 ]
 
 
