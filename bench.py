@@ -260,6 +260,7 @@ def main():
     ap.add_argument("--workload", default="ultra64k")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dense-steps", type=int, default=3)
+    ap.add_argument("--no-fidelity", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -447,6 +448,43 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1)) / e2e_steps
+    del xin, xout, hout
+
+    # ---- fidelity diagnostics (BA-Att §3.1 Eq. 3, §3.2 Eq. 5-8) -------------
+    # The share of the dense attention mass the headline selection keeps
+    # (mean recall), with the norm sort and without it, and how well the
+    # bound U of Eq. 8 tracks the observed token-vs-block logit deviation
+    # (correlation over block pairs: a synthetic analogue of the paper's
+    # Fig. 2).  Timed: one ba_block_fidelity call (S = Q K^T over every tile
+    # pair on the tensor cores + the exp sums).
+    fid = dict()
+    if not args.no_fidelity:
+        _, lse_dense = bsb.ba_attn_dense(qd, kd, vd)
+        bsb.ba_select_into(qd, kd, B, kappa, 1.0, 3, 0, perm_q, perm_k, idx, mask, None, ws_sel)
+        bsb.ba_block_fidelity(qd, kd, B, lse_dense, perm_q, perm_k, idx)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        f_sorted = bsb.ba_block_fidelity(qd, kd, B, lse_dense, perm_q, perm_k, idx)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        fid_ms = e0.elapsed_time(e1)
+        sel0 = bsb.ba_select(qd, kd, B, kappa, 1.0, bsb.SORT_NONE)
+        f_plain = bsb.ba_block_fidelity(qd, kd, B, lse_dense, sel0["perm_q"], sel0["perm_k"],
+                                        sel0["block_idx"])
+        torch.cuda.synchronize(dev)
+
+        def corr(fd):
+            x, y = fd["bound"].flatten().double(), fd["dev_max"].flatten().double()
+            return float(torch.corrcoef(torch.stack([x, y]))[0, 1])
+        s_flops = 2.0 * b * h * L * L * d
+        fid = dict(fidelity_ms=round(fid_ms, 3),
+                   fidelity_s_tflops=round(s_flops / (fid_ms * 1e-3) / 1e12, 1),
+                   recall_mean_sorted=round(float(f_sorted["recall"].double().mean()), 4),
+                   recall_mean_unsorted=round(float(f_plain["recall"].double().mean()), 4),
+                   bound_dev_corr_sorted=round(corr(f_sorted), 4),
+                   bound_dev_corr_unsorted=round(corr(f_plain), 4),
+                   dev_over_bound_sorted=round(float((f_sorted["dev_max"] / f_sorted["bound"]).double().mean()), 4))
+        del f_sorted, f_plain, sel0, lse_dense
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
@@ -485,6 +523,7 @@ def main():
             speedup_vs_dense=round(dense_ms / ms_step, 3),
             isolated_select_ms=round(iso_ms, 4),
             isolated_select=f"prefill {pre} tokens, kappa {kpre} + {kgen}, sort QK",
+            **fid,
             density=round(attn_flops / flops_step, 4)),
     )
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -20,7 +20,7 @@ import re
 from . import _build
 
 __all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_select_isolated",
-           "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into",
+           "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into", "ba_block_fidelity",
            "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
            "last_device_error", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
@@ -47,6 +47,9 @@ _SIGS = {
     "ba_merge_lse": (_c_int, [_c_void_p] * 4 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
     "ba_select_isolated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 8 + [_c_float, _c_int, _c_int]
                            + [_c_void_p] * 6 + [_c_size, _c_void_p]),
+    "ba_block_fidelity_workspace_size": (_c_size, [_c_int] * 5),
+    "ba_block_fidelity": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 5 + [_c_void_p] * 3 + [_c_float]
+                          + [_c_void_p, _c_int] + [_c_void_p] * 5 + [_c_size, _c_void_p]),
     "ba_select_noalloc": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int]
                           + [_c_void_p] * 5 + [_c_void_p]),
 }
@@ -181,6 +184,34 @@ def ba_select_isolated(q, k, block, prefill_len, kappa_prefill, kappa_generation
     if not return_scores:
         del out["block_scores"]
     return out
+
+
+def ba_block_fidelity(q, k, block, lse, perm_q=None, perm_k=None, block_idx=None, scale=0.0,
+                      deviation=True, bound=True):
+    """Fidelity diagnostics of a selection (BA-Att §3.1 Eq. 3, §3.2 Eq. 5-8)
+    over the sorted blocks of perm_q / perm_k (None = identity).  ``lse`` is
+    the dense row LSE from ba_attn_dense.  Returns a dict with mass (fp32
+    [b,h,N,N], Eq. 3), and as asked dev_max and bound ([b,h,N,N]) and recall
+    ([b,h,N], when ``block_idx`` is given)."""
+    torch = _torch()
+    lib = load()
+    _need_cuda(q, k, lse, perm_q, perm_k, block_idx)
+    b, h, L, d = q.shape
+    N = -(-L // block)
+    dev = q.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(mass=torch.empty((b, h, N, N), **f32),
+               dev_max=torch.empty((b, h, N, N), **f32) if deviation else None,
+               bound=torch.empty((b, h, N, N), **f32) if bound else None,
+               recall=torch.empty((b, h, N), **f32) if block_idx is not None else None)
+    kappa = 0 if block_idx is None else block_idx.shape[-1]
+    ws = _workspace(int(lib.ba_block_fidelity_workspace_size(b, h, L, d, block)), dev)
+    ws_bytes = ws.numel() * ws.element_size()
+    st = lib.ba_block_fidelity(_ptr(q), _ptr(k), b, h, L, d, block, _ptr(perm_q), _ptr(perm_k), _ptr(lse),
+                               float(scale), _ptr(block_idx), kappa, _ptr(out["mass"]), _ptr(out["dev_max"]),
+                               _ptr(out["bound"]), _ptr(out["recall"]), _ptr(ws), ws_bytes, _stream(dev))
+    _check(st, "ba_block_fidelity")
+    return {kk: vv for kk, vv in out.items() if vv is not None}
 
 
 def ba_select_noalloc_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, perm_k,

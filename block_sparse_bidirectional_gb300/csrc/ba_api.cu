@@ -192,6 +192,53 @@ int ba_select_isolated(const void *q, const void *k, int batch, int heads, int s
   return map_cuda(run_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t ba_block_fidelity_workspace_size(int batch, int heads, int seqlen, int head_dim, int block) {
+  if (check_shape(batch, heads, seqlen, head_dim, block) != BA_OK) return 0;
+  return fidelity_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim, block);
+}
+
+int ba_block_fidelity(const void *q, const void *k, int batch, int heads, int seqlen,
+                      int head_dim, int block, const int32_t *perm_q, const int32_t *perm_k,
+                      const float *lse, float scale, const int32_t *block_idx, int kappa,
+                      float *mass, float *dev_max, float *bound, float *recall, void *workspace,
+                      size_t workspace_bytes, ba_stream_t stream) {
+  int st = check_shape(batch, heads, seqlen, head_dim, block);
+  if (st != BA_OK) return st;
+  const int n = (seqlen + block - 1) / block;
+  if (!isfinite(scale)) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !lse || !mass) return BA_ERR_INVALID_ARG;
+  if (recall && (!block_idx || kappa < 1 || kappa > n)) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(lse) || !aligned16(mass) ||
+      (dev_max && !aligned16(dev_max)) || (bound && !aligned16(bound)) ||
+      (recall && !aligned16(recall)) || (perm_q && !aligned16(perm_q)) ||
+      (perm_k && !aligned16(perm_k)) || (block_idx && !aligned16(block_idx)))
+    return BA_ERR_INVALID_ARG;
+  const size_t need = ba_block_fidelity_workspace_size(batch, heads, seqlen, head_dim, block);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return BA_ERR_WORKSPACE;
+  FidArgs a;
+  a.q = q;
+  a.k = k;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = block;
+  a.perm_q = perm_q;
+  a.perm_k = perm_k;
+  a.lse = lse;
+  a.scale = scale;
+  a.block_idx = block_idx;
+  a.kappa = kappa;
+  a.mass = mass;
+  a.dev_max = dev_max;
+  a.bound = bound;
+  a.recall = recall;
+  a.workspace = workspace;
+  return map_cuda(run_fidelity(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t ba_sparse_attn_workspace_size(int batch, int heads, int seqlen, int head_dim, int block,
                                      int kappa, int has_perm_q, int has_perm_k) {
   (void)kappa;
@@ -279,8 +326,10 @@ int ba_merge_lse(const void *o1, const float *lse1, const void *o2, const float 
 int ba_last_device_error(ba_stream_t stream, uint32_t *detail) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BA_ERR_CUDA;
-  uint32_t word = 0;
+  uint32_t word = 0, fid = 0;
   if (take_attn_error_word(&word) != cudaSuccess) return BA_ERR_CUDA;
+  if (take_fidelity_error_word(&fid) != cudaSuccess) return BA_ERR_CUDA;
+  if (word == 0) word = fid;
   if (detail) *detail = word;
   return (word & 1u) ? BA_ERR_DEVICE_TIMEOUT : BA_OK;
 }

@@ -34,6 +34,23 @@ struct AttnArgs {
   void *workspace;
 };
 
+// Fidelity diagnostics (block mass, logit deviation, its bound, recall).
+struct FidArgs {
+  const void *q, *k;
+  int batch, heads, seqlen, head_dim, block;
+  const int32_t *perm_q, *perm_k;  // nullable: identity
+  const float *lse;                // dense row LSE [b,h,L], original order
+  float scale;
+  const int32_t *block_idx;        // nullable unless recall is asked for
+  int kappa;
+  float *mass, *dev_max, *bound, *recall;
+  void *workspace;
+};
+
+size_t fidelity_workspace_bytes(int64_t bh, int L, int D, int B);
+cudaError_t run_fidelity(const FidArgs &a, cudaStream_t st);
+cudaError_t take_fidelity_error_word(uint32_t *word);
+
 size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode);
 cudaError_t run_select(const SelectArgs &a, cudaStream_t st);
 

@@ -206,6 +206,46 @@ int ba_sparse_attn(const void *q, const void *k, const void *v, int batch,
                    ba_stream_t stream);
 
 /*
+ * Fidelity diagnostics of a block selection (BA-Att paper §3.1 Eq. 3 and
+ * §3.2 Eq. 5-8), all over the sorted blocks that perm_q / perm_k define
+ * (NULL = identity), with s_ij = q_i.k_j and the scale of the attention call
+ * (<= 0 selects 1/sqrt(d)):
+ *   mass[gq,gk]    = (1/|I(gq)|) sum_{i in I(gq), j in J(gk)} exp(scale s_ij - lse_i),
+ *                    the oracle block mass of Eq. 3 (lse = the dense row
+ *                    log-sum-exp, as ba_attn_dense writes it, original order);
+ *   dev_max[gq,gk] = max_{i in I(gq), j in J(gk)} |scale s_ij - scale Qbar_gq.Kbar_gk|,
+ *                    the largest token-vs-block logit deviation (Eq. 5);
+ *   bound[gq,gk]   = scale (R^Q M^K + M^Q R^K + R^Q R^K), Eq. 7-8 (R the
+ *                    block radii max ||x - mean||, M the block max norms);
+ *   recall[gq]     = sum over the kappa blocks of block_idx[gq] of mass[gq,.],
+ *                    the share of the dense attention mass a selection keeps.
+ * Each row of mass sums to 1 up to rounding.
+ *
+ * q, k        bf16 [b,h,L,d], device.
+ * lse         fp32 [b,h,L], device (required).
+ * block_idx   int32 [b,h,N,kappa] (required when recall != NULL).
+ * mass        fp32 [b,h,N,N] (required); dev_max, bound: fp32 [b,h,N,N] or
+ *             NULL; recall: fp32 [b,h,N] or NULL.
+ * workspace   ba_block_fidelity_workspace_size() bytes, 256-byte aligned:
+ *             permuted row copies, block means, radii and norms, block logits.
+ * Uses tcgen05 tensor-core MMAs for s (bf16 in, fp32 accumulate); mass and
+ * dev_max are accumulated with atomics, so mass may differ in the last bits
+ * between runs.  Errors as in ba_sparse_attn; bounded waits report through
+ * ba_last_device_error.
+ */
+size_t ba_block_fidelity_workspace_size(int batch, int heads, int seqlen,
+                                        int head_dim, int block);
+
+int ba_block_fidelity(const void *q, const void *k, int batch, int heads,
+                      int seqlen, int head_dim, int block,
+                      const int32_t *perm_q, const int32_t *perm_k,
+                      const float *lse, float scale,
+                      const int32_t *block_idx, int kappa, float *mass,
+                      float *dev_max, float *bound, float *recall,
+                      void *workspace, size_t workspace_bytes,
+                      ba_stream_t stream);
+
+/*
  * Dense attention with the same kernel (every key block of every row, no
  * permutation): softmax(scale * Q K^T) V and its row LSE — the BA-Att
  * paper's Eq. 1, the dense reference its speedups are measured against.

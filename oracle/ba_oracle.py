@@ -421,6 +421,25 @@ def oracle_block_mass(q, k, perm_q, perm_k, B, scale=None):
     return out
 
 
+def observed_deviation(q, k, perm_q, perm_k, B, scale=None):
+    """§3.2: the largest |l_hat_ij - l_{gq,gk}| over the token pairs of each
+    block pair, l_hat_ij = scale * q_i.k_j (Eq. 5's left side) and l the
+    block logit of Eq. 2 with the same scale (1/sqrt(d) by default)."""
+    L, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    qs, ks = q[perm_q], k[perm_k]
+    qbar, _ = block_moments(qs, B)
+    kbar, _ = block_moments(ks, B)
+    rng = block_ranges(L, B)
+    out = np.empty((len(rng), len(rng)))
+    for g, (a, b_) in enumerate(rng):
+        for j, (c, e) in enumerate(rng):
+            tok = scale * (qs[a:b_] @ ks[c:e].T)
+            out[g, j] = np.abs(tok - scale * (qbar[g] @ kbar[j])).max()
+    return out
+
+
 def deviation_bound(q, k, perm_q, perm_k, B):
     """Eq. 7-8: radii R, max norms M and the bound U[gq, gk] on |l_hat_ij - l|."""
     L, d = q.shape

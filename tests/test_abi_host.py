@@ -127,6 +127,46 @@ def test_select_isolated_rejects(kw, status):
     assert _select_iso(bsb.load(), **kw) == status
 
 
+def _fid(lib, **kw):
+    a = dict(q=P, k=P, b=1, h=1, L=1024, d=64, B=64, pq=P2, pk=P2, lse=P, scale=0.0, idx=P2, kappa=8,
+             mass=P, dev=P, bound=P, recall=P, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return lib.ba_block_fidelity(a["q"], a["k"], a["b"], a["h"], a["L"], a["d"], a["B"], a["pq"], a["pk"],
+                                 a["lse"], a["scale"], a["idx"], a["kappa"], a["mass"], a["dev"],
+                                 a["bound"], a["recall"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(lse=None), INVALID),
+    (dict(mass=None), INVALID),
+    (dict(q=None), INVALID),
+    (dict(idx=None), INVALID),          # recall asked for without a list
+    (dict(kappa=0), INVALID),
+    (dict(kappa=17), INVALID),
+    (dict(dev=MIS), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(d=96), UNSUPPORTED),
+    (dict(B=32), UNSUPPORTED),
+    (dict(ws_bytes=1024), WORKSPACE),
+    (dict(ws=None), WORKSPACE),
+])
+def test_fidelity_rejects(kw, status):
+    assert _fid(bsb.load(), **kw) == status
+
+
+def test_fidelity_workspace_size():
+    lib = bsb.load()
+    b, h, L, d, B = 1, 4, 1000, 128, 64
+    N = -(-L // B)
+
+    def a256(x):
+        return (x + 255) // 256 * 256
+    want = (2 * a256(b * h * L * d * 2) + 2 * a256(b * h * N * d * 4) + 4 * a256(b * h * N * 4)
+            + a256(b * h * N * N * 4))
+    assert lib.ba_block_fidelity_workspace_size(b, h, L, d, B) == want
+    assert lib.ba_block_fidelity_workspace_size(b, h, L, 96, B) == 0
+
+
 def _attn(lib, **kw):
     a = dict(q=P, k=P, v=P, b=1, h=1, L=1024, d=64, B=64, pq=P2, pk=P2, idx=P2, kappa=8, scale=0.0,
              o=P, lse=P, ws=P, ws_bytes=1 << 30, stream=None)

@@ -135,6 +135,27 @@ def check_deviation_bound():
                         assert dev <= bnd["U"][gq, gk] + 1e-12
 
 
+def check_deviation_hand_example():
+    """Eq. 7-8 and the observed deviation on the hand-worked example: radii,
+    max norms, U and the largest token-vs-block logit gap, each worked out
+    by hand (tests/golden/hand_example.json, unsorted blocks)."""
+    with open(os.path.join(GOLDEN, "hand_example.json")) as f:
+        ex = json.load(f)
+    Q = np.array(ex["Q"], float)
+    K = np.array(ex["K"], float)
+    part = ex["unsorted"]
+    ev = lambda x: eval(str(x), {"sqrt": math.sqrt})  # noqa: E731 (hand-written expressions)
+    p = np.arange(4)
+    bnd = O.deviation_bound(Q, K, p, p, 2)
+    for key in ("RQ", "MQ", "RK", "MK"):
+        np.testing.assert_allclose(bnd[key], [ev(x) for x in part["radii"][key]], atol=1e-12)
+    want_u = np.array([[ev(x) for x in row] for row in part["U_times_sqrt_d"]]) / math.sqrt(2)
+    np.testing.assert_allclose(bnd["U"], want_u, atol=1e-12)
+    dev = O.observed_deviation(Q, K, p, p, 2)
+    np.testing.assert_allclose(dev, np.array(part["max_dev_dot"], float) / math.sqrt(2), atol=1e-12)
+    assert np.all(dev <= bnd["U"] + 1e-12)
+
+
 def check_topk_bruteforce():
     """Algorithm 1 steps 8-11 by brute force, with exact ties (integer scores)."""
     rng = _rng(5)
@@ -334,7 +355,7 @@ ALL_CHECKS = [check_hand_example, check_sort_bruteforce, check_block_logit_bilin
               check_topk_equals_softmax_order, check_all_blocks_is_dense_attention,
               check_constant_v, check_masked_softmax_bruteforce, check_lse_merge,
               check_ragged_tail_moments, check_kappa_rule, check_block_mass,
-              check_isolated_sort, check_isolated_topk_bruteforce,
+              check_isolated_sort, check_isolated_topk_bruteforce, check_deviation_hand_example,
               check_isolated_keeps_generation_block]
 
 
