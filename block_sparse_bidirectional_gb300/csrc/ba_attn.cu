@@ -54,6 +54,7 @@ template <int BK> struct RegSplit { static constexpr int kLow = 72, kHigh = 216;
 template <> struct RegSplit<64> { static constexpr int kLow = 104, kHigh = 200; };
 static_assert(4 * 32 * RegSplit<128>::kLow + 8 * 32 * RegSplit<128>::kHigh == 384 * 168, "split");
 static_assert(4 * 32 * RegSplit<64>::kLow + 8 * 32 * RegSplit<64>::kHigh == 384 * 168, "split");
+constexpr int kSplitRegs(int lo, int hi) { return 4 * 32 * lo + 8 * 32 * hi; }
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxBlocks = 4096;
 
@@ -714,6 +715,12 @@ static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, con
     e = cudaFuncSetAttribute(k_attn<D, BK, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay::kAlloc);
     if (e != cudaSuccess) return e;
+    // setmaxnreg.inc draws on the registers the block is launched with: a
+    // split larger than that pool would never be granted, so refuse it here
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, k_attn<D, BK, kDense>)) != cudaSuccess) return e;
+    if (fa.numRegs * kAttnThreads < kSplitRegs(RegSplit<BK>::kLow, RegSplit<BK>::kHigh))
+      return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
   const dim3 grid((p.n_tiles + kTiles - 1) / kTiles, static_cast<unsigned>(bh));
