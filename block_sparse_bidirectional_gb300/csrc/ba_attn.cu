@@ -6,7 +6,9 @@
 // A CTA owns two tiles of 128 consecutive sorted query rows.  A tile is one
 // query block when B = 128, two when B = 64 (then it walks the union of the
 // two lists, each entry tagged with which block selected it; rows of the
-// other block see -inf for that entry).
+// other block see -inf for that entry).  Key blocks are always consumed as
+// 128-key slots: with B = 64 two list entries share a slot (two 64-row
+// boxes), so every iteration has the shape of the B = 128 path.
 //
 // Warp roles (384 threads; setmaxnreg moves registers to the softmax warps):
 //   warp 0       TMA producer: both Q tiles once, then every K_j and V_j
@@ -48,12 +50,8 @@ constexpr int kTiles = 2;            // query tiles per CTA (ping-pong)
 constexpr int kAttnThreads = 384;    // 12 warps
 // Registers per thread after setmaxnreg: warps 0-3 drop to kLow, warps 4-11
 // rise to kHigh; 4*32*kLow + 8*32*kHigh must equal the launch's 384*168.
-// 64-key tiles hold more pointer state in the producer/MMA warps and fewer
-// S columns per softmax thread, so they split differently.
 template <int BK> struct RegSplit { static constexpr int kLow = 72, kHigh = 216; };
-template <> struct RegSplit<64> { static constexpr int kLow = 104, kHigh = 200; };
 static_assert(4 * 32 * RegSplit<128>::kLow + 8 * 32 * RegSplit<128>::kHigh == 384 * 168, "split");
-static_assert(4 * 32 * RegSplit<64>::kLow + 8 * 32 * RegSplit<64>::kHigh == 384 * 168, "split");
 constexpr int kSplitRegs(int lo, int hi) { return 4 * 32 * lo + 8 * 32 * hi; }
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxBlocks = 4096;
@@ -169,7 +167,7 @@ __device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pa
   }
 }
 
-template <int D, int BK, bool kDense>
+template <int D, int BK, bool kDense, bool kPack>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
@@ -234,11 +232,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  const int n_t[kTiles] = {static_cast<int>(misc[1]), static_cast<int>(misc[2])};
+  // Packed mode (64-token blocks): list entries are taken two at a time, one
+  // 128-key slot holding the two 64-key blocks, so iteration j covers
+  // entries 2j and 2j + 1 (the second is a fully masked dummy past the end).
+  const int ne[kTiles] = {static_cast<int>(misc[1]), static_cast<int>(misc[2])};
+  const int n_t[kTiles] = {kPack ? (ne[0] + 1) / 2 : ne[0], kPack ? (ne[1] + 1) / 2 : ne[1]};
   const int nmax = max(n_t[0], n_t[1]);
-  // Positions j < n_common hold the same block in both tiles' lists (dense:
-  // every position), so the K_j / V_j load is shared by the two tiles there.
-  const int n_common = kDense ? (n_t[1] > 0 ? n_t[0] : 0) : static_cast<int>(misc[4]);
+  // Positions j < n_common hold the same block(s) in both tiles' lists
+  // (dense: every position), so the K_j / V_j load is shared there.
+  const int n_common = kDense ? (n_t[1] > 0 ? n_t[0] : 0)
+                              : (kPack ? static_cast<int>(misc[4]) / 2 : static_cast<int>(misc[4]));
 
   if (warp < 4) {
     reg_dealloc<RegSplit<BK>::kLow>();
@@ -263,15 +266,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       int issued = 0;
       auto load = [&](bool is_v, int t, int j) -> bool {
-        const int blk = kDense ? j : (plist[t][j] & 0xFFF);
+        int blk, blk_b = 0;
+        if (kPack) {
+          blk = plist[t][2 * j] & 0xFFF;
+          blk_b = (2 * j + 1 < ne[t]) ? (plist[t][2 * j + 1] & 0xFFF) : blk;
+        } else {
+          blk = kDense ? j : (plist[t][j] & 0xFFF);
+        }
         const int s = issued % S;
         if (issued >= S && !mbar_wait(&slot_empty[s], ((issued / S) & 1) ^ 1u, kSiteKEmpty, abort_flag))
           return false;
         mbar_arrive_expect_tx(&slot_full[s], Lay::kSlotBytes);
+        const CUtensorMap *map = is_v ? &tmV : &tmK;
+        uint8_t *dst = sSlot + s * Lay::kSlotBytes;
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sSlot + s * Lay::kSlotBytes + c * BK * 128, is_v ? &tmV : &tmK, &slot_full[s],
-                      c * 64, blk * BK, bh);
+        for (int c = 0; c < D / 64; ++c) {
+          if (kPack) {
+            // rows 0-63 from block a, rows 64-127 from block b (64-row boxes)
+            tma_load_3d(dst + c * BK * 128, map, &slot_full[s], c * 64, blk * (BK / 2), bh);
+            tma_load_3d(dst + c * BK * 128 + (BK / 2) * 128, map, &slot_full[s], c * 64,
+                        blk_b * (BK / 2), bh);
+          } else {
+            tma_load_3d(dst + c * BK * 128, map, &slot_full[s], c * 64, blk * BK, bh);
+          }
+        }
         ++issued;
         return true;
       };
@@ -382,7 +400,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tO = tmem + lane_base + kTiles * BK + t * D;
     const int row_sorted = (tile0 + t) * kTileM + r;
     const bool row_valid = row_sorted < p.L;
-    const int my_g = r / BK;
+    const int my_g = r / (kPack ? BK / 2 : BK);
     const float cl = p.scale_log2;
     const uint64_t cl2 = f2_pack(cl, cl);
     float m = -INFINITY;
@@ -398,19 +416,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // entries (64-row blocks) or the ragged last key block.  With 128-row
     // blocks every entry of a tile's list is its own, so when L is a multiple
     // of 128 the list is never read here.
-    const bool read_list = !kDense && (BK < kTileM || p.L % BK != 0);
+    const bool read_list = !kDense && (kPack || BK < kTileM || p.L % BK != 0);
     uint32_t my_e = 0;  // sparse: 32 list entries at a time, one per lane
     for (int j = 0; j < n; ++j) {
-      uint32_t e;
-      if (read_list) {
+      uint32_t e, eb = 0;
+      if (kPack) {
+        // entries 2j, 2j + 1; a missing second entry reads 0 (no selection bit)
+        if ((j & 15) == 0) my_e = (2 * j + lane < ne[t]) ? __ldg(plist[t] + 2 * j + lane) : 0u;
+        e = __shfl_sync(0xffffffffu, my_e, (2 * j) & 31);
+        eb = __shfl_sync(0xffffffffu, my_e, (2 * j + 1) & 31);
+      } else if (read_list) {
         if ((j & 31) == 0) my_e = (j + lane < n) ? __ldg(plist[t] + j + lane) : 0u;
         e = __shfl_sync(0xffffffffu, my_e, j & 31);
       } else {
         e = kDense ? dense_entry(j) : 0u;  // sparse: block 0, never the ragged one
       }
       const int blk = e & 0xFFF;
-      const bool sel = (BK == kTileM) || ((e >> (12 + my_g)) & 1u);
-      const int valid_cols = min(BK, p.L - blk * BK);
+      const bool sel = (!kPack && BK == kTileM) || ((e >> (12 + my_g)) & 1u);
+      // packed: columns [0, BK/2) belong to block a (e), [BK/2, BK) to block b (eb)
+      const int bsz = kPack ? BK / 2 : BK;
+      const int valid_cols = min(bsz, p.L - blk * bsz);
+      const bool sel_b = kPack && ((eb >> (12 + my_g)) & 1u);
+      const int valid_b = kPack ? min(bsz, p.L - static_cast<int>(eb & 0xFFF) * bsz) : 0;
       ok = mbar_wait(&s_full[t], j & 1, kSiteSFull, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -418,15 +445,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
       for (int c = 0; c < BK / 32; ++c) tmem_ld32(tS + c * 32, sv + c * 32);
       tmem_wait_ld();
-      if (!sel || valid_cols < BK) {
+      float mx, mx_b = -INFINITY;
+      if (kPack) {
+        if (!sel || valid_cols < bsz) {
 #pragma unroll
-        for (int c = 0; c < BK; ++c)
-          if (!sel || c >= valid_cols) sv[c] = -INFINITY;
+          for (int c = 0; c < BK / 2; ++c)
+            if (!sel || c >= valid_cols) sv[c] = -INFINITY;
+        }
+        if (!sel_b || valid_b < bsz) {
+#pragma unroll
+          for (int c = 0; c < BK / 2; ++c)
+            if (!sel_b || c >= valid_b) sv[BK / 2 + c] = -INFINITY;
+        }
+        mx = sv[0];
+#pragma unroll
+        for (int c = 1; c + 1 < BK / 2; c += 2) mx = max3f(mx, sv[c], sv[c + 1]);
+        mx = fmaxf(mx, sv[BK / 2 - 1]);
+        mx_b = sv[BK / 2];
+#pragma unroll
+        for (int c = BK / 2 + 1; c + 1 < BK; c += 2) mx_b = max3f(mx_b, sv[c], sv[c + 1]);
+        mx_b = fmaxf(mx_b, sv[BK - 1]);
+      } else {
+        if (!sel || valid_cols < BK) {
+#pragma unroll
+          for (int c = 0; c < BK; ++c)
+            if (!sel || c >= valid_cols) sv[c] = -INFINITY;
+        }
+        mx = sv[0];
+#pragma unroll
+        for (int c = 1; c + 1 < BK; c += 2) mx = max3f(mx, sv[c], sv[c + 1]);
+        mx = fmaxf(mx, sv[BK - 1]);
       }
-      float mx = sv[0];
-#pragma unroll
-      for (int c = 1; c + 1 < BK; c += 2) mx = max3f(mx, sv[c], sv[c + 1]);
-      mx = fmaxf(mx, sv[BK - 1]);
+      // the two blocks' maxima (packed) keep their own rounding corrections
+      const float mx_a = mx;
+      if (kPack) mx = fmaxf(mx, mx_b);
       const float m_new = fmaxf(m, mx * cl);
       const bool need = m_new > m + kRescaleLog2;
       const bool resc = need && (m != -INFINITY);
@@ -456,8 +508,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t nm2 = f2_pack(nm, nm);
       {
         // computed exactly as this element's P entry below (same fma, ex2, RN)
-        const float pbm = fast_exp2(fmaf(mx, cl, nm));
+        const float pbm = fast_exp2(fmaf(mx_a, cl, nm));
         lcorr += __bfloat162float(__float2bfloat16_rn(pbm)) - pbm;
+        if (kPack) {
+          const float pbb = fast_exp2(fmaf(mx_b, cl, nm));
+          lcorr += __bfloat162float(__float2bfloat16_rn(pbb)) - pbb;
+        }
       }
       // P_j overwrites the first BK/2 columns of S_j (bf16 pairs), 32 at a time
 #pragma unroll
@@ -703,7 +759,7 @@ static int gather_lookahead(int npairs) {
   return (2 * sms + npairs - 1) / npairs;
 }
 
-template <int D, int BK, bool kDense>
+template <int D, int BK, bool kDense, bool kPack = false>
 static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                const AttnParams &p, int64_t bh, cudaStream_t st) {
   using Lay = AttnLayout<D, BK>;
@@ -712,19 +768,19 @@ static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, con
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_attn<D, BK, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(k_attn<D, BK, kDense, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Lay::kAlloc);
     if (e != cudaSuccess) return e;
     // setmaxnreg.inc draws on the registers the block is launched with: a
     // split larger than that pool would never be granted, so refuse it here
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, k_attn<D, BK, kDense>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, k_attn<D, BK, kDense, kPack>)) != cudaSuccess) return e;
     if (fa.numRegs * kAttnThreads < kSplitRegs(RegSplit<BK>::kLow, RegSplit<BK>::kHigh))
       return cudaErrorInvalidConfiguration;
     configured_device = dev;
   }
   const dim3 grid((p.n_tiles + kTiles - 1) / kTiles, static_cast<unsigned>(bh));
-  k_attn<D, BK, kDense><<<grid, kAttnThreads, Lay::kAlloc, st>>>(mq, mk, mv, p);
+  k_attn<D, BK, kDense, kPack><<<grid, kAttnThreads, Lay::kAlloc, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -801,6 +857,7 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   }
   alignas(64) CUtensorMap mq, mk, mv;
   if ((e = encode_tensor_map_3d(&mq, qs, D, L, bh, 64, kTileM)) != cudaSuccess) return e;
+  // 64-token blocks are loaded as 64-row boxes, two per 128-key slot
   if ((e = encode_tensor_map_3d(&mk, ks, D, L, bh, 64, BK)) != cudaSuccess) return e;
   if ((e = encode_tensor_map_3d(&mv, vs, D, L, bh, 64, BK)) != cudaSuccess) return e;
 
@@ -833,9 +890,9 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
     if (D == 64) return launch_attn<64, 128, true>(mq, mk, mv, p, bh, st);
   } else {
     if (D == 128 && BK == 128) return launch_attn<128, 128, false>(mq, mk, mv, p, bh, st);
-    if (D == 128 && BK == 64) return launch_attn<128, 64, false>(mq, mk, mv, p, bh, st);
+    if (D == 128 && BK == 64) return launch_attn<128, 128, false, true>(mq, mk, mv, p, bh, st);
     if (D == 64 && BK == 128) return launch_attn<64, 128, false>(mq, mk, mv, p, bh, st);
-    if (D == 64 && BK == 64) return launch_attn<64, 64, false>(mq, mk, mv, p, bh, st);
+    if (D == 64 && BK == 64) return launch_attn<64, 128, false, true>(mq, mk, mv, p, bh, st);
   }
   return cudaErrorInvalidValue;
 }
