@@ -49,7 +49,7 @@ def peaks():
 # DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
 # of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
 # for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
-ATTN_TRAFFIC = {"ultra64k": dict(bytes=5269495040, kernel_sha="f0f712c269d7876f")}
+ATTN_TRAFFIC = {"ultra64k": dict(bytes=5219350016, kernel_sha="1d5a7eae8a15c3f3")}
 
 
 def attn_traffic(workload: str):
