@@ -370,6 +370,30 @@ def main():
     dense_ms = e0.elapsed_time(e1) / args.dense_steps
     del od, lsed
 
+    # ---- LoSA locality pruning at the same shape (groups of 32, top 4) -------
+    # reads the current and the previous query (2 x b*h*L*d bf16): HBM-bound
+    q_prev = qd.clone()
+    q_prev.view(-1)[::7] += 1
+    act = torch.empty((b, h, L), dtype=torch.uint8, device=dev)
+    lib = bsb.load()
+    pq_ptr, pp_ptr = bsb._ptr(qd), bsb._ptr(q_prev)
+    st_ptr = bsb._stream(dev)
+
+    def losa():
+        r = lib.ba_active_tokens(pq_ptr, pp_ptr, b, h, L, d, 32, 4, bsb._ptr(act), None, st_ptr)
+        if r != 0:
+            raise RuntimeError(f"ba_active_tokens status {r}")
+    losa()
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(5):
+        losa()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    losa_ms = e0.elapsed_time(e1) / 5
+    losa_bytes = 2 * qd.numel() * qd.element_size() + act.numel()
+    del q_prev, act
+
     # ---- isolated selection (SparseD §3.3) at the same shape ----------------
     # the first quarter of the tokens as prompt, half of each part's key blocks
     pre = (L // 4) // B * B
@@ -522,6 +546,9 @@ def main():
             dense_frac_tensor_burst=round(flops_step / (dense_ms * 1e-3) / 1e12 / pk["bf16"], 4),
             speedup_vs_dense=round(dense_ms / ms_step, 3),
             isolated_select_ms=round(iso_ms, 4),
+            active_tokens_ms=round(losa_ms, 4),
+            active_tokens_gbs=round(losa_bytes / (losa_ms * 1e-3) / 1e9, 1),
+            active_tokens_frac_hbm_measured=round(losa_bytes / (losa_ms * 1e-3) / 1e9 / peaks()["hbm"], 4),
             isolated_select=f"prefill {pre} tokens, kappa {kpre} + {kgen}, sort QK",
             **fid,
             density=round(attn_flops / flops_step, 4)),

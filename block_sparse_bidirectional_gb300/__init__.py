@@ -21,6 +21,7 @@ from . import _build
 
 __all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_select_isolated",
            "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into", "ba_block_fidelity",
+           "ba_active_tokens", "ba_reuse_rows",
            "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
            "last_device_error", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
@@ -50,6 +51,8 @@ _SIGS = {
     "ba_block_fidelity_workspace_size": (_c_size, [_c_int] * 5),
     "ba_block_fidelity": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 5 + [_c_void_p] * 3 + [_c_float]
                           + [_c_void_p, _c_int] + [_c_void_p] * 5 + [_c_size, _c_void_p]),
+    "ba_active_tokens": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_void_p, _c_void_p, _c_void_p]),
+    "ba_reuse_rows": (_c_int, [_c_void_p] * 3 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
     "ba_select_noalloc": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 6 + [_c_float, _c_int, _c_int]
                           + [_c_void_p] * 5 + [_c_void_p]),
 }
@@ -212,6 +215,34 @@ def ba_block_fidelity(q, k, block, lse, perm_q=None, perm_k=None, block_idx=None
                                _ptr(out["bound"]), _ptr(out["recall"]), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "ba_block_fidelity")
     return {kk: vv for kk, vv in out.items() if vv is not None}
+
+
+def ba_active_tokens(q_now, q_prev, group, top_k, return_mse=False):
+    """LoSA locality pruning: uint8 [b,h,L] mask of the top_k tokens per
+    group of ``group`` whose queries moved most between two steps (and the
+    fp32 per-token MSE with ``return_mse``)."""
+    torch = _torch()
+    lib = load()
+    _need_cuda(q_now, q_prev)
+    b, h, L, d = q_now.shape
+    active = torch.empty((b, h, L), dtype=torch.uint8, device=q_now.device)
+    mse = torch.empty((b, h, L), dtype=torch.float32, device=q_now.device) if return_mse else None
+    st = lib.ba_active_tokens(_ptr(q_now), _ptr(q_prev), b, h, L, d, group, top_k, _ptr(active),
+                              _ptr(mse), _stream(q_now.device))
+    _check(st, "ba_active_tokens")
+    return (active, mse) if return_mse else active
+
+
+def ba_reuse_rows(o_new, lse_new, active, o_cache, lse_cache):
+    """LoSA cache update in place: active rows of o_cache / lse_cache take
+    o_new / lse_new."""
+    lib = load()
+    _need_cuda(o_new, lse_new, active, o_cache, lse_cache)
+    d = o_new.shape[-1]
+    rows = o_new.numel() // d
+    st = lib.ba_reuse_rows(_ptr(o_new), _ptr(lse_new), _ptr(active), rows, d, _ptr(o_cache),
+                           _ptr(lse_cache), _stream(o_new.device))
+    _check(st, "ba_reuse_rows")
 
 
 def ba_select_noalloc_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, perm_k,

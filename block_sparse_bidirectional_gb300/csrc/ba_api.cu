@@ -192,6 +192,31 @@ int ba_select_isolated(const void *q, const void *k, int batch, int heads, int s
   return map_cuda(run_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ba_active_tokens(const void *q_now, const void *q_prev, int batch, int heads, int seqlen,
+                     int head_dim, int group, int top_k, uint8_t *active, float *mse,
+                     ba_stream_t stream) {
+  if (batch < 1 || heads < 1 || seqlen < 1) return BA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return BA_ERR_UNSUPPORTED;
+  if (group < 1 || group > kLosaMaxGroup || top_k < 1) return BA_ERR_INVALID_ARG;
+  const int64_t bh = static_cast<int64_t>(batch) * heads;
+  if (bh > 65535) return BA_ERR_UNSUPPORTED;
+  if (!q_now || !q_prev || !active) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q_now) || !aligned16(q_prev) || (mse && !aligned16(mse))) return BA_ERR_INVALID_ARG;
+  return map_cuda(run_active_tokens(q_now, q_prev, bh, seqlen, head_dim, group, top_k, active, mse,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int ba_reuse_rows(const void *o_new, const float *lse_new, const uint8_t *active, int64_t rows,
+                  int head_dim, void *o_cache, float *lse_cache, ba_stream_t stream) {
+  if (rows < 0) return BA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return BA_ERR_UNSUPPORTED;
+  if (rows == 0) return BA_OK;
+  if (!o_new || !lse_new || !active || !o_cache || !lse_cache) return BA_ERR_INVALID_ARG;
+  if (!aligned16(o_new) || !aligned16(o_cache)) return BA_ERR_INVALID_ARG;
+  return map_cuda(run_reuse_rows(o_new, lse_new, active, rows, head_dim, o_cache, lse_cache,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t ba_block_fidelity_workspace_size(int batch, int heads, int seqlen, int head_dim, int block) {
   if (check_shape(batch, heads, seqlen, head_dim, block) != BA_OK) return 0;
   return fidelity_workspace_bytes(static_cast<int64_t>(batch) * heads, seqlen, head_dim, block);

@@ -34,6 +34,13 @@ struct AttnArgs {
   void *workspace;
 };
 
+// LoSA locality pruning and result reuse.
+constexpr int kLosaMaxGroup = 1024;
+cudaError_t run_active_tokens(const void *q_now, const void *q_prev, int64_t bh, int L, int D,
+                              int group, int top_k, uint8_t *active, float *mse, cudaStream_t st);
+cudaError_t run_reuse_rows(const void *o_new, const float *lse_new, const uint8_t *active,
+                           int64_t rows, int D, void *o_cache, float *lse_cache, cudaStream_t st);
+
 // Fidelity diagnostics (block mass, logit deviation, its bound, recall).
 struct FidArgs {
   const void *q, *k;

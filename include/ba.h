@@ -206,6 +206,39 @@ int ba_sparse_attn(const void *q, const void *k, const void *v, int batch,
                    ba_stream_t stream);
 
 /*
+ * LoSA locality pruning (the LoSA summary post, step 1): between two
+ * denoising steps, per group of `group` consecutive tokens of each (b,h)
+ * sequence (the block denoised in parallel; the last group may be short),
+ * the `top_k` tokens whose query vectors changed most are active:
+ *     mse[i]    = (1/d) sum_t (q_now[i,t] - q_prev[i,t])^2     (fp32)
+ *     active[i] = 1 iff fewer than top_k tokens of i's group have a larger
+ *                 mse, or an equal one at a lower index; else 0.
+ * Stable tokens keep their cached attention result (see ba_reuse_rows);
+ * active ones take a new one.
+ *
+ * q_now, q_prev  bf16 [b,h,L,d], device, 16-byte aligned.
+ * group          1 <= group <= 1024; top_k >= 1 (top_k >= group: all active).
+ * active         uint8 [b,h,L] output; mse: fp32 [b,h,L] output or NULL.
+ * Errors: BA_ERR_INVALID_ARG (null or misaligned pointers, bad group or
+ * top_k, empty shape), BA_ERR_UNSUPPORTED (d not 64/128, b*h > 65535).
+ */
+int ba_active_tokens(const void *q_now, const void *q_prev, int batch,
+                     int heads, int seqlen, int head_dim, int group,
+                     int top_k, uint8_t *active, float *mse,
+                     ba_stream_t stream);
+
+/*
+ * The cache update of a LoSA step ("merge and update"): for every row r with
+ * active[r] != 0, o_cache[r] = o_new[r] and lse_cache[r] = lse_new[r];
+ * stable rows keep their cached values.  rows = b*h*L.
+ * o_new, o_cache  bf16 [rows, d] (d = 64 or 128), device, 16-byte aligned;
+ * lse_new, lse_cache fp32 [rows]; active uint8 [rows].  rows == 0 is a no-op.
+ */
+int ba_reuse_rows(const void *o_new, const float *lse_new,
+                  const uint8_t *active, int64_t rows, int head_dim,
+                  void *o_cache, float *lse_cache, ba_stream_t stream);
+
+/*
  * Fidelity diagnostics of a block selection (BA-Att paper §3.1 Eq. 3 and
  * §3.2 Eq. 5-8), all over the sorted blocks that perm_q / perm_k define
  * (NULL = identity), with s_ij = q_i.k_j and the scale of the attention call

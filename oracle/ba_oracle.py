@@ -400,6 +400,44 @@ def merge_lse(O1, lse1, O2, lse2):
 
 
 # ---------------------------------------------------------------------------
+# LoSA locality pruning and result reuse (the LoSA summary post, steps 1, 2
+# and the cache update of step 4)
+# ---------------------------------------------------------------------------
+#
+# Between two denoising steps most tokens' queries barely move.  Per block of
+# ``group`` consecutive tokens (the block that is denoised in parallel), the
+# ``top_k`` tokens whose query vectors changed most (mean squared error over
+# the d features) are "active"; the rest are "stable" and keep the attention
+# result (O and its log-normaliser) cached from the previous step.  Ties go to
+# the lower token index; a short last group keeps min(top_k, its length).
+
+def query_mse(q_now: np.ndarray, q_prev: np.ndarray) -> np.ndarray:
+    """Per token: (1/d) * sum_t (q_now[t] - q_prev[t])^2, over the last axis."""
+    diff = q_now - q_prev
+    return np.mean(diff * diff, axis=-1)
+
+
+def active_tokens(mse: np.ndarray, group: int, top_k: int) -> np.ndarray:
+    """Boolean mask [L]: the top_k largest ``mse`` of every run of ``group``
+    tokens (ties to the lower index)."""
+    L = mse.shape[0]
+    out = np.zeros(L, dtype=bool)
+    for g0 in range(0, L, group):
+        seg = mse[g0:g0 + group]
+        order = np.lexsort((np.arange(len(seg)), -seg))
+        out[g0 + order[:min(top_k, len(seg))]] = True
+    return out
+
+
+def reuse_rows(o_new, lse_new, o_cache, lse_cache, active):
+    """The cache after a LoSA step: active rows take the new result, stable
+    rows keep the cached one."""
+    o = np.where(active[..., None], o_new, o_cache)
+    lse = np.where(active, lse_new, lse_cache)
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
 # Fidelity diagnostics (BA-Att paper §3.1 Eq. 3 and §3.2 Eq. 7-8)
 # ---------------------------------------------------------------------------
 

@@ -167,6 +167,41 @@ def test_fidelity_workspace_size():
     assert lib.ba_block_fidelity_workspace_size(b, h, L, 96, B) == 0
 
 
+def _act(lib, **kw):
+    a = dict(qn=P, qp=P, b=1, h=2, L=1000, d=128, group=32, k=4, act=P2, mse=None, stream=None)
+    a.update(kw)
+    return lib.ba_active_tokens(a["qn"], a["qp"], a["b"], a["h"], a["L"], a["d"], a["group"], a["k"],
+                                a["act"], a["mse"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qn=None), INVALID),
+    (dict(qp=MIS), INVALID),
+    (dict(act=None), INVALID),
+    (dict(group=0), INVALID),
+    (dict(group=1025), INVALID),
+    (dict(k=0), INVALID),
+    (dict(L=0), INVALID),
+    (dict(d=96), UNSUPPORTED),
+])
+def test_active_tokens_rejects(kw, status):
+    assert _act(bsb.load(), **kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(o_new=None), INVALID),
+    (dict(o_cache=MIS), INVALID),
+    (dict(act=None), INVALID),
+    (dict(rows=-1), INVALID),
+    (dict(d=32), UNSUPPORTED),
+])
+def test_reuse_rows_rejects(kw, status):
+    a = dict(o_new=P, lse_new=P, act=P2, rows=100, d=64, o_cache=P, lse_cache=P, stream=None)
+    a.update(kw)
+    assert bsb.load().ba_reuse_rows(a["o_new"], a["lse_new"], a["act"], a["rows"], a["d"],
+                                    a["o_cache"], a["lse_cache"], a["stream"]) == status
+
+
 def _attn(lib, **kw):
     a = dict(q=P, k=P, v=P, b=1, h=1, L=1024, d=64, B=64, pq=P2, pk=P2, idx=P2, kappa=8, scale=0.0,
              o=P, lse=P, ws=P, ws_bytes=1 << 30, stream=None)

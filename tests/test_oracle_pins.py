@@ -156,6 +156,44 @@ def check_deviation_hand_example():
     assert np.all(dev <= bnd["U"] + 1e-12)
 
 
+def check_active_tokens():
+    """LoSA locality pruning: the MSE is the plain per-token mean of squared
+    differences (checked entry by entry in pure Python), each group keeps
+    exactly min(top_k, group length) tokens, and those are the ones no other
+    token of the group beats (larger MSE, or equal MSE and lower index) --
+    brute force over integer-valued changes with ties."""
+    rng = _rng(41)
+    L, d = 37, 3
+    prev = rng.integers(-2, 3, (L, d)).astype(float)
+    now = prev + rng.integers(-1, 2, (L, d)).astype(float)
+    mse = O.query_mse(now, prev)
+    for i in range(L):
+        assert mse[i] == sum((now[i, t] - prev[i, t]) ** 2 for t in range(d)) / d
+    for group, k in ((8, 3), (5, 5), (16, 1), (37, 10)):
+        act = O.active_tokens(mse, group, k)
+        for g0 in range(0, L, group):
+            idx = list(range(g0, min(L, g0 + group)))
+            assert int(act[idx].sum()) == min(k, len(idx))
+            for i in idx:
+                beaten = sum(1 for j in idx if mse[j] > mse[i] or (mse[j] == mse[i] and j < i))
+                assert act[i] == (beaten < k)
+    # with exactly top_k moved tokens in every group, the active set is them
+    now2 = prev.copy()
+    moved = [1, 6, 9, 14, 17, 20, 25, 30, 33, 35]
+    now2[moved] += 1.0
+    act2 = O.active_tokens(O.query_mse(now2, prev), 8, 2)
+    assert np.nonzero(act2)[0].tolist() == moved
+
+
+def check_reuse_rows():
+    """Active rows take the new result, stable rows keep the cache."""
+    o_new, o_c = np.full((4, 2), 1.0), np.full((4, 2), 2.0)
+    l_new, l_c = np.array([1.0, 1, 1, 1]), np.array([2.0, 2, 2, 2])
+    act = np.array([True, False, True, False])
+    o, l = O.reuse_rows(o_new, l_new, o_c, l_c, act)
+    assert o[:, 0].tolist() == [1, 2, 1, 2] and l.tolist() == [1, 2, 1, 2]
+
+
 def check_topk_bruteforce():
     """Algorithm 1 steps 8-11 by brute force, with exact ties (integer scores)."""
     rng = _rng(5)
@@ -356,6 +394,7 @@ ALL_CHECKS = [check_hand_example, check_sort_bruteforce, check_block_logit_bilin
               check_constant_v, check_masked_softmax_bruteforce, check_lse_merge,
               check_ragged_tail_moments, check_kappa_rule, check_block_mass,
               check_isolated_sort, check_isolated_topk_bruteforce, check_deviation_hand_example,
+              check_active_tokens, check_reuse_rows,
               check_isolated_keeps_generation_block]
 
 
@@ -472,6 +511,21 @@ def _isolated_joint(scores, n_pre, kappa_pre, kappa_gen):
     return O.topk_blocks(scores, kappa_pre + kappa_gen)
 
 
+def _mse_sum(q_now, q_prev):
+    diff = q_now - q_prev
+    return np.sum(diff * diff, axis=-1)
+
+
+def _active_high_tie(mse, group, top_k):
+    L = mse.shape[0]
+    out = np.zeros(L, dtype=bool)
+    for g0 in range(0, L, group):
+        seg = mse[g0:g0 + group]
+        order = np.lexsort((-np.arange(len(seg)), -seg))
+        out[g0 + order[:min(top_k, len(seg))]] = True
+    return out
+
+
 _ORIG = {n: getattr(O, n) for n in ("block_moments", "covariance_compensation", "block_logits",
                                       "topk_blocks", "norm_sort_permutation", "sparse_attention_one",
                                       "split_sort_permutation", "topk_blocks_isolated")}
@@ -490,6 +544,8 @@ MUTANTS = [
     ("split_sort_permutation", _split_sort_whole),
     ("topk_blocks_isolated", _isolated_no_offset),
     ("topk_blocks_isolated", _isolated_joint),
+    ("query_mse", _mse_sum),
+    ("active_tokens", _active_high_tie),
 ]
 
 
