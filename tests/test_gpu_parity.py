@@ -252,3 +252,45 @@ def test_merge_lse_kernel_joins_split_lists(dev):
     om, lm = bsb.ba_merge_lse(o1, l1, o2, l2)
     torch.cuda.synchronize()
     check_attention(to64(om), lm.cpu().double().numpy(), to64(o), l.cpu().double().numpy())
+
+
+def test_step_captures_in_a_cuda_graph(dev):
+    """A whole select + sparse-attention step (norm pass, sort, statistics,
+    scores, top-kappa, pair lists, gathers, attention) records into a CUDA
+    graph and replays to the same bits as eager execution: the calls only
+    enqueue kernels on the caller's stream and take every buffer from it."""
+    b, h, L, d, B, kappa = 1, 4, 4096, 128, 128, 8
+    q, k, v = workloads.random_inputs(b, h, L, d, seed=91, scale=1.5)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    N = -(-L // B)
+    i32 = dict(dtype=torch.int32, device=dev)
+    pq, pk = torch.empty((b, h, L), **i32), torch.empty((b, h, L), **i32)
+    idx, mask = torch.empty((b, h, N, kappa), **i32), torch.empty((b, h, N, -(-N // 32)), **i32)
+    wss = torch.empty(bsb.select_workspace_size(b, h, L, d, B, kappa), dtype=torch.uint8, device=dev)
+    wsa = torch.empty(bsb.sparse_attn_workspace_size(b, h, L, d, B, kappa), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((b, h, L), dtype=torch.float32, device=dev)
+
+    def step():
+        bsb.ba_select_into(qd, kd, B, kappa, 1.0, bsb.SORT_QK, 0, pq, pk, idx, mask, None, wss)
+        bsb.ba_sparse_attn_into(qd, kd, vd, B, pq, pk, idx, 0.0, o, lse, wsa)
+
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        step()                       # eager, also configures the kernels once
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in (pq, pk, idx, o, lse)]
+    for t in (o, lse):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        for a, r in zip((pq, pk, idx, o, lse), ref):
+            assert torch.equal(a, r)
+    st, word = bsb.last_device_error()
+    assert st == 0, hex(word)
