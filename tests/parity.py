@@ -6,6 +6,9 @@ The tolerances are the ones the method's acceptance criteria state:
   * O: max |err| <= 2e-2 and mean |err| <= 2e-3 against the oracle evaluated
     on the GPU's permutation and mask (bf16 inputs, fp32 accumulation);
   * LSE: |err| <= 1e-3.
+Block scores l' = a . b are fp32 dot products of length 3d on the GPU; their
+rounding error grows with the dot product's condition sum_t |a_t b_t| (which
+bounds |l'|), so they are compared to 2e-5 of max(row max |l'|, that sum).
 Permutations come from fp32 squared norms on the GPU and fp64 norms in the
 oracle: where norms are within rounding of each other several orders are
 correct, so the check is that the GPU's pi is a permutation, sorted under the
@@ -18,6 +21,7 @@ from __future__ import annotations
 import numpy as np
 
 MASK_REL = 1e-4
+SCORE_REL = 2e-5
 O_MAX, O_MEAN, LSE_TOL = 2e-2, 2e-3, 1e-3
 NORM_REL = 1e-5
 
@@ -114,3 +118,33 @@ def check_attention(o_gpu, lse_gpu, o_ref, lse_ref, rows=None):
     assert stats["o_mean"] <= O_MEAN, stats
     assert stats["lse_max"] <= LSE_TOL, stats
     return stats
+
+
+def score_condition(Q64, K64, perm_q, perm_k, B, beta):
+    """sum_t |a_t b_t| per block pair [b,h,N,N] for the augmented vectors of
+    Eq. 13-14 (a = [Qbar/sqrt(d), beta/d VarQ, beta/d Qbar^2],
+    b = [Kbar, Kbar^2 + VarK, VarK]), from the oracle's fp64 block moments on
+    the given permutations."""
+    import oracle.ba_oracle as O
+
+    b, h, L, d = Q64.shape
+    N = O.num_blocks(L, B)
+    out = np.empty((b, h, N, N))
+    for bi in range(b):
+        for hi in range(h):
+            qbar, varq = O.block_moments(Q64[bi, hi][perm_q[bi, hi]], B)
+            kbar, vark = O.block_moments(K64[bi, hi][perm_k[bi, hi]], B)
+            c = np.abs(qbar) @ np.abs(kbar).T / np.sqrt(d)
+            c += abs(beta) / d * (varq @ (kbar * kbar + vark).T + (qbar * qbar) @ vark.T)
+            out[bi, hi] = c
+    return out
+
+
+def check_scores(scores_gpu, scores_oracle, Q64, K64, perm_q, perm_k, B, beta):
+    """|l'_gpu - l'_oracle| <= SCORE_REL * max(row max |l'|, sum_t |a_t b_t|)."""
+    sg = scores_gpu.astype(np.float64)
+    so = scores_oracle
+    row = np.maximum(np.abs(so).max(axis=-1, keepdims=True), 1e-6)
+    scale = np.maximum(row, score_condition(Q64, K64, perm_q, perm_k, B, beta))
+    err = np.abs(sg - so)
+    assert np.all(err <= SCORE_REL * scale), float((err / scale).max())

@@ -17,7 +17,7 @@ import torch
 import block_sparse_bidirectional_gb300 as bsb
 import oracle.ba_oracle as O
 import workloads
-from parity import MASK_REL, NORM_REL, check_attention, check_perm, to64
+from parity import MASK_REL, NORM_REL, check_attention, check_perm, check_scores, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -107,9 +107,8 @@ def _isolated_and_check(q, k, B, prefill, kpre, kgen, beta, mode, window, dev):
         assert np.array_equal(g["perm_q"], np.broadcast_to(np.arange(L), g["perm_q"].shape))
     ora = O.ba_select_isolated(Q64, K64, B, prefill, kpre, kgen, beta, mode, window,
                                perm_q=g["perm_q"], perm_k=g["perm_k"])
-    so, sgs = ora["scores"], g["block_scores"].astype(np.float64)
-    scale = np.maximum(np.abs(so).max(axis=-1, keepdims=True), 1e-6)
-    assert np.all(np.abs(sgs - so) <= 2e-5 * scale)
+    so = ora["scores"]
+    check_scores(g["block_scores"], so, Q64, K64, g["perm_q"], g["perm_k"], B, beta)
     _check_isolated_lists(g, so, prefill // B, kpre, kgen)
     return sel, g
 

@@ -13,7 +13,7 @@ import torch
 import block_sparse_bidirectional_gb300 as bsb
 import oracle.ba_oracle as O
 import workloads
-from parity import check_attention, check_mask, check_perm, check_topk_of_own_scores, to64
+from parity import check_attention, check_mask, check_perm, check_scores, check_topk_of_own_scores, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -39,9 +39,8 @@ def test_max_block_count(dev, d, B, kappa):
     check_perm(g["perm_q"], own["perm_q"], Q64)
     check_perm(g["perm_k"], own["perm_k"], K64)
     ora = O.ba_select(Q64, K64, B, kappa, 1.0, O.SORT_QK, perm_q=g["perm_q"], perm_k=g["perm_k"])
-    so, sg = ora["scores"], g["block_scores"].astype(np.float64)
-    scale = np.maximum(np.abs(so).max(axis=-1, keepdims=True), 1e-6)
-    assert np.all(np.abs(sg - so) <= 2e-5 * scale)
+    so = ora["scores"]
+    check_scores(g["block_scores"], so, Q64, K64, g["perm_q"], g["perm_k"], B, 1.0)
     check_topk_of_own_scores(g["block_idx"], g["block_scores"], kappa)
     check_mask(g["block_idx"], g["block_mask"], so, kappa, g["block_scores"])
     o, lse = bsb.ba_sparse_attn(qd, kd, vd, B, sel["perm_q"], sel["perm_k"], sel["block_idx"])

@@ -17,7 +17,8 @@ import torch
 import block_sparse_bidirectional_gb300 as bsb
 import oracle.ba_oracle as O
 import workloads
-from parity import (check_attention, check_mask, check_perm, check_topk_of_own_scores, to64)
+from parity import (check_attention, check_mask, check_perm, check_scores, check_topk_of_own_scores,
+                    to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -45,9 +46,8 @@ def _select_and_check(q, k, B, kappa, beta, mode, window, dev):
     else:
         assert np.array_equal(g["perm_k"], np.broadcast_to(np.arange(q.shape[2]), g["perm_k"].shape))
     ora = O.ba_select(Q64, K64, B, kappa, beta, mode, window, perm_q=g["perm_q"], perm_k=g["perm_k"])
-    so, sg = ora["scores"], g["block_scores"].astype(np.float64)
-    scale = np.maximum(np.abs(so).max(axis=-1, keepdims=True), 1e-6)
-    assert np.all(np.abs(sg - so) <= 2e-5 * scale), float((np.abs(sg - so) / scale).max())
+    so = ora["scores"]
+    check_scores(g["block_scores"], so, Q64, K64, g["perm_q"], g["perm_k"], B, beta)
     check_topk_of_own_scores(g["block_idx"], g["block_scores"], kappa)
     check_mask(g["block_idx"], g["block_mask"], so, kappa, g["block_scores"])
     return sel, g
@@ -76,6 +76,8 @@ SMALL = [
     (1, 1, 50, 128, 64, 1),
     (1, 2, 4096, 128, 128, 32),
     (1, 1, 4160, 64, 64, 20),
+    (1, 1, 1, 64, 64, 1),       # a single token: O = V, LSE = scale * q.k
+    (2, 2, 1, 128, 128, 1),
 ]
 
 
@@ -102,7 +104,8 @@ def test_custom_scale(dev):
     _attn_and_check(q, k, v, 128, sel, g, dev, scale=0.05)
 
 
-@pytest.mark.parametrize("shape", [(1, 2, 1024, 64), (2, 3, 1000, 128), (1, 1, 77, 64), (1, 2, 3000, 128)])
+@pytest.mark.parametrize("shape", [(1, 2, 1024, 64), (2, 3, 1000, 128), (1, 1, 77, 64), (1, 2, 3000, 128),
+                                   (2, 1, 1, 128)])
 def test_dense_against_oracle(dev, shape):
     b, h, L, d = shape
     q, k, v = workloads.random_inputs(b, h, L, d, seed=L * d)
