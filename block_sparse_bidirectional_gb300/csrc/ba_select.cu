@@ -20,7 +20,8 @@
 //                     b = [Kbar, Kbar^2 + VarK, VarK]
 //                   so that a.b = Eq. 2 + beta * Eq. 14 (Eq. 13).
 //   k_scores        l'[gq,gk] = a_gq . b_gk: a batched fp32 SIMT GEMM
-//                   (128x128 tiles, 8x8 register micro-tiles, f32x2 FMAs).  Kept on the
+//                   (128x128 tiles, 8x8 outputs per thread in a
+//                   conflict-free fragment layout, f32x2 FMAs).  Kept on the
 //                   fp32 ALUs so the top-kappa decision is taken in fp32.
 //   k_topk          steps 8-11: one warp per query-block row, keys held in
 //                   registers; MSB-first radix
@@ -449,8 +450,12 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
 
 // ---------------------------------------------------------------------------
 // step 5-7: scores = A . B^T per (b,h); A, B are [N][KS] rows with stride 3D.
-// grid = (ceil(N/128), ceil(N/128), b*h); 128x128 tiles, 8x8 register
-// micro-tiles, packed f32x2 FMAs.
+// grid = (ceil(N/128), ceil(N/128), b*h); 128x128 tiles, 8x8 outputs per
+// thread, packed f32x2 FMAs.  A warp covers 4 x 8 threads of the 16 x 16
+// thread grid; a thread owns rows {4ty..4ty+3, 64+4ty..64+4ty+3} and the
+// same pattern of columns, so each fragment load of a warp is one
+// shared-memory wavefront (broadcast for A, 128 contiguous bytes for B).
+// Every output is one fma chain over k in order.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
                                                 const float *__restrict__ Bm,
@@ -464,7 +469,8 @@ __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
   const float *Bb = Bm + bh * N * static_cast<int64_t>(stride);
   const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BM;
   const int tid = threadIdx.x;
-  const int tx = tid % 16, ty = tid / 16;
+  const int warp = tid / 32, lane = tid % 32;
+  const int tx = (warp % 2) * 8 + lane % 8, ty = (warp / 2) * 4 + lane / 8;
   const int lr = tid / 2, lk = (tid % 2) * 4;  // loader: row, k offset
   uint64_t acc[8][4];
 #pragma unroll
@@ -487,10 +493,10 @@ __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < BKK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][ty * 8]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][ty * 8 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 8]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 8 + 4]);
+      const float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][64 + tx * 4]);
       const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
       const uint64_t bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
                               f2_pack(b1.z, b1.w)};
@@ -503,18 +509,29 @@ __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
     }
     __syncthreads();
   }
+  // row r < 4: 4ty + r, else 64 + 4ty + r - 4; pair c < 2: columns 4tx + 2c,
+  // + 1, else 64 + 4tx + 2(c - 2), + 1
   float *Cb = C + bh * N * static_cast<int64_t>(N);
+  const bool vec = (N % 4) == 0;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    const int i = i0 + ty * 8 + r;
+    const int i = i0 + (r < 4 ? ty * 4 + r : 64 + ty * 4 + r - 4);
     if (i >= N) continue;
+    float *crow = Cb + i * static_cast<int64_t>(N);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float x0, x1;
-      f2_unpack(acc[r][c], x0, x1);
-      const int j = j0 + tx * 8 + 2 * c;
-      if (j < N) Cb[i * static_cast<int64_t>(N) + j] = x0;
-      if (j + 1 < N) Cb[i * static_cast<int64_t>(N) + j + 1] = x1;
+    for (int half = 0; half < 2; ++half) {
+      const int j = j0 + half * 64 + tx * 4;
+      float x0, x1, x2, x3;
+      f2_unpack(acc[r][2 * half], x0, x1);
+      f2_unpack(acc[r][2 * half + 1], x2, x3);
+      if (vec && j + 3 < N) {
+        *reinterpret_cast<float4 *>(crow + j) = make_float4(x0, x1, x2, x3);
+      } else {
+        if (j < N) crow[j] = x0;
+        if (j + 1 < N) crow[j + 1] = x1;
+        if (j + 2 < N) crow[j + 2] = x2;
+        if (j + 3 < N) crow[j + 3] = x3;
+      }
     }
   }
 }

@@ -78,6 +78,8 @@ SMALL = [
     (1, 1, 4160, 64, 64, 20),
     (1, 1, 1, 64, 64, 1),       # a single token: O = V, LSE = scale * q.k
     (2, 2, 1, 128, 128, 1),
+    (1, 2, 129, 64, 64, 2),     # last block of one token (packed 64-token path)
+    (1, 1, 4097, 128, 128, 5),  # last block of one token (128-token path)
 ]
 
 
