@@ -65,7 +65,9 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
 #pragma unroll
   for (int u = 0; u < kNormRowsPerThread; ++u) {
     const int64_t row = row0 + u * RPW;
-    raw[u] = (row < rows) ? __ldg(reinterpret_cast<const uint4 *>(x + row * D) + part)
+    // read once here (the block statistics gather these rows again much
+    // later, long after they left L2): streaming loads
+    raw[u] = (row < rows) ? __ldcs(reinterpret_cast<const uint4 *>(x + row * D) + part)
                           : make_uint4(0, 0, 0, 0);
   }
 #pragma unroll
@@ -549,7 +551,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // The row is split in two parts, elements [0, n_first) with budget
 // kappa_first and [n_first, N) with budget kappa - kappa_first (isolated
 // prefill / generation selection); n_first == N is the plain top-kappa.
-template <int KPL>
+// kRange = false: the part is the whole row; elements past N hold key 0,
+// which no candidate (>= 1) counts, so no range test is needed.
+template <int KPL, bool kRange>
 __device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int lane, int lo, int hi,
                                                int k, uint32_t &T, int &need) {
   T = 0;
@@ -559,7 +563,7 @@ __device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int 
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
       const int e = i * 32 + lane;
-      cnt += (e >= lo && e < hi) && keys[i] >= cand;
+      cnt += (!kRange || (e >= lo && e < hi)) && keys[i] >= cand;
     }
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (cnt >= static_cast<uint32_t>(k)) T = cand;
@@ -568,7 +572,7 @@ __device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int 
 #pragma unroll
   for (int i = 0; i < KPL; ++i) {
     const int e = i * 32 + lane;
-    gt += (e >= lo && e < hi) && keys[i] > T;
+    gt += (!kRange || (e >= lo && e < hi)) && keys[i] > T;
   }
   gt = __reduce_add_sync(0xffffffffu, gt);
   need = k - static_cast<int>(gt);  // >= 1 keys equal to T to take, lowest index first
@@ -592,9 +596,13 @@ __global__ void __launch_bounds__(kTopkWarps * 32) k_topk(const float *__restric
   }
   uint32_t T0, T1 = 0;
   int need0, need1 = 0;
-  part_threshold<KPL>(keys, lane, 0, n_first, kappa_first, T0, need0);
   const bool two = n_first < N;
-  if (two) part_threshold<KPL>(keys, lane, n_first, N, kappa - kappa_first, T1, need1);
+  if (two) {
+    part_threshold<KPL, true>(keys, lane, 0, n_first, kappa_first, T0, need0);
+    part_threshold<KPL, true>(keys, lane, n_first, N, kappa - kappa_first, T1, need1);
+  } else {
+    part_threshold<KPL, false>(keys, lane, 0, N, kappa_first, T0, need0);
+  }
   const int nwords = (N + 31) / 32;
   const uint32_t lt_mask = (1u << lane) - 1u;
   int taken0 = 0, taken1 = 0, base = 0;
