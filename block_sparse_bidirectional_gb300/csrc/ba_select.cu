@@ -366,13 +366,14 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
     const int32_t *__restrict__ perm_q, const int32_t *__restrict__ perm_k, int L, int N,
     float *__restrict__ aug_q, float *__restrict__ aug_k, float beta) {
   constexpr int VPR = D / 8;             // 16-byte vectors per row
-  constexpr int P = kStatsThreads / D;   // row slices per feature
+  constexpr int QPR = D / 4;             // 4-feature groups per row
+  constexpr int P = kStatsThreads / QPR; // row slices
   extern __shared__ __align__(16) unsigned char st_raw[];
   __nv_bfloat16 *stage[2] = {reinterpret_cast<__nv_bfloat16 *>(st_raw),
                              reinterpret_cast<__nv_bfloat16 *>(st_raw) + BK * D};
   int *s_src = reinterpret_cast<int *>(st_raw + 2 * BK * D * 2);  // [bpc][BK]
-  __shared__ float red[P][D];
-  __shared__ float s_mean[D];
+  __shared__ __align__(16) float red[P][D];
+  __shared__ __align__(16) float s_mean[D];
   const bool qside = blockIdx.z == 0;
   const __nv_bfloat16 *x = qside ? xq : xk;
   const int32_t *perm = qside ? perm_q : perm_k;
@@ -398,7 +399,17 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
     cp_async_commit();
   };
   issue(0);
-  const int dim = threadIdx.x % D, part = threadIdx.x / D;
+  // a thread sums 4 features over the rows part, part + P, ...; a warp reads
+  // whole rows (8-byte loads); the P partial sums of a feature are then
+  // added in slice order by one thread
+  const int quad = threadIdx.x % QPR, part = threadIdx.x / QPR;
+  const int dim = threadIdx.x;  // feature owned in the combine step (< D)
+  auto load4 = [&](const __nv_bfloat16 *rows, int r, float (&f)[4]) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(rows + r * D + quad * 4);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+    f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+  };
   for (int bi = 0; bi < nblk; ++bi) {
     if (bi + 1 < nblk) {
       issue(bi + 1);
@@ -410,9 +421,14 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
     const __nv_bfloat16 *rows = stage[bi & 1];
     const int g = g0 + bi;
     const int n = min(BK, L - g * BK);
-    float acc = 0.f;
-    for (int r = part; r < n; r += P) acc += __bfloat162float(rows[r * D + dim]);
-    red[part][dim] = acc;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = part; r < n; r += P) {
+      float f[4];
+      load4(rows, r, f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] += f[c];
+    }
+    *reinterpret_cast<float4 *>(&red[part][quad * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
     if (threadIdx.x < D) {
       float sum = 0.f;
@@ -421,19 +437,27 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
       s_mean[dim] = sum / static_cast<float>(n);
     }
     __syncthreads();
-    const float mean = s_mean[dim];
-    acc = 0.f;
+    const float4 m4 = *reinterpret_cast<const float4 *>(&s_mean[quad * 4]);
+    const float mq[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = 0.f;
     for (int r = part; r < n; r += P) {
-      const float dv = __bfloat162float(rows[r * D + dim]) - mean;
-      acc = fmaf(dv, dv, acc);
+      float f[4];
+      load4(rows, r, f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float dv = f[c] - mq[c];
+        acc[c] = fmaf(dv, dv, acc[c]);
+      }
     }
-    red[part][dim] = acc;
+    *reinterpret_cast<float4 *>(&red[part][quad * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
     if (threadIdx.x < D) {
       float sum = 0.f;
 #pragma unroll
       for (int q = 0; q < P; ++q) sum += red[q][dim];
       const float var = sum / static_cast<float>(n);
+      const float mean = s_mean[dim];
       float *o = aug + (bh * N + g) * static_cast<int64_t>(3 * D);
       if (qside) {
         const float cf = beta / static_cast<float>(D);
