@@ -5,9 +5,9 @@
 //   k_sqnorm_keys   Eq. 9: fp32 squared norm of every Q / K row, packed with
 //                   the token index into a 64-bit sort key.  One streaming
 //                   pass over Q and K (16-byte vector loads, coalesced).
-//   k_chunk_sort    Eq. 10: 4096-key chunks: each warp sorts 256 keys in
-//                   registers (bitonic network, shuffles), the CTA merges the
-//                   runs in shared memory.
+//   k_chunk_sort    Eq. 10: 4096-key chunks: each thread sorts 8 keys in
+//                   registers (a 19-comparator network), the CTA merges the
+//                   runs in shared memory (merge path, 9 levels).
 //   k_merge_pass    merge-path merge of sorted runs (width doubles per pass);
 //                   the last pass emits pi (sorted position -> token index).
 //                   Keys are unique (index in the low word), so the result is
@@ -92,9 +92,9 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
 
 // ---------------------------------------------------------------------------
 // step 1-2b: chunk sort.  grid = (chunks per window, windows, sorted sequences)
-// A warp sorts 256 keys in registers (bitonic network, 8 keys per lane,
-// shuffles across lanes); the CTA then merges the 16 runs in shared memory
-// (merge path, 4 levels).  Keys are unique, so the order is the stable one.
+// A thread sorts its 8 consecutive keys in registers; the CTA then merges
+// the 512 runs in shared memory (merge path, 9 levels).  Keys are unique,
+// so the order is the stable one.
 // ---------------------------------------------------------------------------
 struct SortGeom {
   int L;        // tokens per sequence
@@ -182,53 +182,30 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
   if (c0 >= wlen) return;  // uniform over the CTA
   const int n = min(kChunk, wlen - c0);
   const int64_t base = static_cast<int64_t>(seq) * g.L + window_start(g, w) + c0;
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  // ---- warp-level bitonic sort of 256 keys; element e = i * 32 + lane ----
-  // (striped, so the loads coalesce).  Partner e ^ j: lane ^ j for j < 32,
-  // register i ^ (j / 32) for j >= 32.
+  // ---- each thread sorts its 8 consecutive keys in registers (Batcher's
+  // odd-even merge network, 19 compare-exchanges) ----
   uint64_t r[8];
-  const int w0 = warp * 256;
+  const int e0 = threadIdx.x * 8;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int e = w0 + i * 32 + lane;
-    r[i] = (e < n) ? keys_in[base + e] : ~0ull;
-  }
+  for (int i = 0; i < 8; ++i) r[i] = (e0 + i < n) ? keys_in[base + e0 + i] : ~0ull;
+  auto cx = [&](int i, int j) {
+    const uint64_t a = r[i], b = r[j];
+    r[i] = a < b ? a : b;
+    r[j] = a < b ? b : a;
+  };
+  cx(0, 1); cx(2, 3); cx(4, 5); cx(6, 7);
+  cx(0, 2); cx(1, 3); cx(4, 6); cx(5, 7);
+  cx(1, 2); cx(5, 6);
+  cx(0, 4); cx(1, 5); cx(2, 6); cx(3, 7);
+  cx(2, 4); cx(3, 5);
+  cx(1, 2); cx(3, 4); cx(5, 6);
 #pragma unroll
-  for (int k = 2; k <= 256; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      if (j < 32) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = i * 32 + lane;
-          const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
-          const uint64_t y = __shfl_xor_sync(0xffffffffu, r[i], j);
-          r[i] = keep_min ? (r[i] < y ? r[i] : y) : (r[i] < y ? y : r[i]);
-        }
-      } else {
-        const int ij = j >> 5;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i & ij) continue;
-          const int i2 = i | ij;
-          const bool up = (((i * 32 + lane) & k) == 0);
-          const uint64_t a = r[i], b = r[i2];
-          if ((a > b) == up) {
-            r[i] = b;
-            r[i2] = a;
-          }
-        }
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) sa[spad(w0 + i * 32 + lane)] = r[i];
+  for (int i = 0; i < 8; ++i) sa[spad(e0 + i)] = r[i];
   __syncthreads();
 
-  // ---- merge the 16 sorted runs: 256 -> 512 -> 1024 -> 2048 -> 4096 ----
+  // ---- merge the 512 sorted runs: 8 -> 16 -> ... -> 4096 ----
   uint64_t *src = sa, *dst = sb;
-  for (int width = 256; width < kChunk; width <<= 1) {
+  for (int width = 8; width < kChunk; width <<= 1) {
     const int o0 = threadIdx.x * 8;
     const int p0 = (o0 / (2 * width)) * 2 * width;
     merge_path_8_smem(src, p0, p0 + width, width, width, o0 - p0, 8, dst, o0);
