@@ -32,6 +32,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "ms & dense-equiv TFLOPS, select+sparse attn, L=64k 50% sparsity; select GB/s"
+# The pages' own figure for this path, quoted as context only (other
+# hardware, another baseline kernel, sparsity not stated): BA-Att §4.3,
+# Fig. 4a; §1 gives the same 6.95x at 128K tokens.
+PAGES_SPEEDUP = ("BA-Att (Sort) operator speedup over FlashAttention-2: up to 6.95x at 256K tokens "
+                 "on an NVIDIA A100 80GB, Triton kernels, block 128 (BA-Att section 4.3, Fig. 4a); "
+                 "context only, not comparable to this GB300 measurement")
 UNIT = "TFLOPS (dense-equivalent 4*b*h*L^2*d per step / step time)"
 
 
@@ -554,6 +560,10 @@ def main():
             dense_tflops=round(flops_step / (dense_ms * 1e-3) / 1e12, 2),
             dense_frac_tensor_burst=round(flops_step / (dense_ms * 1e-3) / 1e12 / pk["bf16"], 4),
             speedup_vs_dense=round(dense_ms / ms_step, 3),
+            # selection + sparse attention together, on the computed tiles
+            step_actual_tflops=round(attn_flops / (ms_step * 1e-3) / 1e12, 2),
+            step_frac_tensor_burst=round(attn_flops / (ms_step * 1e-3) / 1e12 / pk["bf16"], 4),
+            pages_speedup_context=PAGES_SPEEDUP,
             isolated_select_ms=round(iso_ms, 4),
             active_tokens_ms=round(losa_ms, 4),
             active_tokens_gbs=round(losa_bytes / (losa_ms * 1e-3) / 1e9, 1),
