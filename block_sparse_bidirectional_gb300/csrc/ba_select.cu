@@ -20,8 +20,9 @@
 //                     b = [Kbar, Kbar^2 + VarK, VarK]
 //                   so that a.b = Eq. 2 + beta * Eq. 14 (Eq. 13).
 //   k_scores        l'[gq,gk] = a_gq . b_gk: a batched fp32 SIMT GEMM
-//                   (128x128 tiles, 8x8 outputs per thread in a
-//                   conflict-free fragment layout, f32x2 FMAs).  Kept on the
+//                   (128x128 tiles, 8x8 outputs per thread, or 64x64 and
+//                   4x4 for small grids, in a conflict-free fragment layout,
+//                   f32x2 FMAs).  Kept on the
 //                   fp32 ALUs so the top-kappa decision is taken in fp32.
 //   k_topk          steps 8-11: one warp per query-block row, keys held in
 //                   registers; MSB-first radix
@@ -453,80 +454,96 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
 
 // ---------------------------------------------------------------------------
 // step 5-7: scores = A . B^T per (b,h); A, B are [N][KS] rows with stride 3D.
-// grid = (ceil(N/128), ceil(N/128), b*h); 128x128 tiles, 8x8 outputs per
-// thread, packed f32x2 FMAs.  A warp covers 4 x 8 threads of the 16 x 16
-// thread grid; a thread owns rows {4ty..4ty+3, 64+4ty..64+4ty+3} and the
-// same pattern of columns, so each fragment load of a warp is one
-// shared-memory wavefront (broadcast for A, 128 contiguous bytes for B).
-// Every output is one fma chain over k in order.
+// grid = (ceil(N/TM), ceil(N/TM), b*h); TM x TM tiles (TM = 128: 8 x 8
+// outputs per thread; TM = 64, for small grids: 4 x 4), packed f32x2 FMAs.
+// A warp covers 4 x 8 threads of the 16 x 16 thread grid; a thread owns the
+// row groups {4ty..4ty+3} (+ TM/2 when TM = 128) and the same pattern of
+// columns, so each fragment load of a warp is one shared-memory wavefront
+// (broadcast for A, 128 contiguous bytes for B).  Every output is one fma
+// chain over k in order, the same for both tile sizes.
 // ---------------------------------------------------------------------------
+template <int TM>
 __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
                                                 const float *__restrict__ Bm,
                                                 float *__restrict__ C, int N, int KS,
                                                 int stride) {
-  constexpr int BM = 128, BKK = 8, PAD = 4;
-  __shared__ __align__(16) float As[BKK][BM + PAD];
-  __shared__ __align__(16) float Bs[BKK][BM + PAD];
+  constexpr int BKK = 8, PAD = 4;
+  constexpr int G = TM / 64;       // 4-row (4-column) groups per thread
+  constexpr int R = 4 * G;         // rows (columns) per thread
+  __shared__ __align__(16) float As[BKK][TM + PAD];
+  __shared__ __align__(16) float Bs[BKK][TM + PAD];
   const int64_t bh = blockIdx.z;
   const float *Ab = A + bh * N * static_cast<int64_t>(stride);
   const float *Bb = Bm + bh * N * static_cast<int64_t>(stride);
-  const int i0 = blockIdx.y * BM, j0 = blockIdx.x * BM;
+  const int i0 = blockIdx.y * TM, j0 = blockIdx.x * TM;
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
   const int tx = (warp % 2) * 8 + lane % 8, ty = (warp / 2) * 4 + lane / 8;
-  const int lr = tid / 2, lk = (tid % 2) * 4;  // loader: row, k offset
-  uint64_t acc[8][4];
+  // loader: TM = 128: every thread one float4 of A and one of B;
+  // TM = 64: threads 0-127 load A, 128-255 load B
+  const int lt = (TM == 128) ? tid : tid % 128;
+  const int lr = lt / 2, lk = (lt % 2) * 4;
+  const bool load_a = (TM == 128) || tid < 128, load_b = (TM == 128) || tid >= 128;
+  uint64_t acc[R][R / 2];
 #pragma unroll
-  for (int r = 0; r < 8; ++r)
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0ull;
+    for (int c = 0; c < R / 2; ++c) acc[r][c] = 0ull;
   const float *arow = Ab + (i0 + lr) * static_cast<int64_t>(stride) + lk;
   const float *brow = Bb + (j0 + lr) * static_cast<int64_t>(stride) + lk;
-  const bool a_ok = i0 + lr < N, b_ok = j0 + lr < N;
-  float4 na4 = a_ok ? *reinterpret_cast<const float4 *>(arow) : make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool a_ok = load_a && i0 + lr < N, b_ok = load_b && j0 + lr < N;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 na4 = a_ok ? *reinterpret_cast<const float4 *>(arow) : z4;
+  float4 nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow) : z4;
   for (int k0 = 0; k0 < KS; k0 += BKK) {
     const float4 va = na4, vb = nb4;
     if (k0 + BKK < KS) {  // prefetch the next chunk while this one is used
-      na4 = a_ok ? *reinterpret_cast<const float4 *>(arow + k0 + BKK) : make_float4(0.f, 0.f, 0.f, 0.f);
-      nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow + k0 + BKK) : make_float4(0.f, 0.f, 0.f, 0.f);
+      na4 = a_ok ? *reinterpret_cast<const float4 *>(arow + k0 + BKK) : z4;
+      nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow + k0 + BKK) : z4;
     }
-    As[lk + 0][lr] = va.x; As[lk + 1][lr] = va.y; As[lk + 2][lr] = va.z; As[lk + 3][lr] = va.w;
-    Bs[lk + 0][lr] = vb.x; Bs[lk + 1][lr] = vb.y; Bs[lk + 2][lr] = vb.z; Bs[lk + 3][lr] = vb.w;
+    if (load_a) {
+      As[lk + 0][lr] = va.x; As[lk + 1][lr] = va.y; As[lk + 2][lr] = va.z; As[lk + 3][lr] = va.w;
+    }
+    if (load_b) {
+      Bs[lk + 0][lr] = vb.x; Bs[lk + 1][lr] = vb.y; Bs[lk + 2][lr] = vb.z; Bs[lk + 3][lr] = vb.w;
+    }
     __syncthreads();
 #pragma unroll
     for (int kk = 0; kk < BKK; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4 *>(&As[kk][ty * 4]);
-      const float4 a1 = *reinterpret_cast<const float4 *>(&As[kk][64 + ty * 4]);
-      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[kk][tx * 4]);
-      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[kk][64 + tx * 4]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const uint64_t bp[4] = {f2_pack(b0.x, b0.y), f2_pack(b0.z, b0.w), f2_pack(b1.x, b1.y),
-                              f2_pack(b1.z, b1.w)};
+      float av[R];
+      uint64_t bp[R / 2];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
+      for (int gi = 0; gi < G; ++gi) {
+        const float4 a4 = *reinterpret_cast<const float4 *>(&As[kk][gi * 64 + ty * 4]);
+        const float4 b4 = *reinterpret_cast<const float4 *>(&Bs[kk][gi * 64 + tx * 4]);
+        av[4 * gi + 0] = a4.x; av[4 * gi + 1] = a4.y; av[4 * gi + 2] = a4.z; av[4 * gi + 3] = a4.w;
+        bp[2 * gi + 0] = f2_pack(b4.x, b4.y);
+        bp[2 * gi + 1] = f2_pack(b4.z, b4.w);
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
         const uint64_t a2 = f2_pack(av[r], av[r]);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = f2_fma(a2, bp[c], acc[r][c]);
+        for (int c = 0; c < R / 2; ++c) acc[r][c] = f2_fma(a2, bp[c], acc[r][c]);
       }
     }
     __syncthreads();
   }
-  // row r < 4: 4ty + r, else 64 + 4ty + r - 4; pair c < 2: columns 4tx + 2c,
-  // + 1, else 64 + 4tx + 2(c - 2), + 1
+  // row r: group r / 4 (offset 64 each), 4ty + r % 4; column pair c: group
+  // c / 2, columns 4tx + 2 (c % 2), + 1
   float *Cb = C + bh * N * static_cast<int64_t>(N);
   const bool vec = (N % 4) == 0;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const int i = i0 + (r < 4 ? ty * 4 + r : 64 + ty * 4 + r - 4);
+  for (int r = 0; r < R; ++r) {
+    const int i = i0 + (r / 4) * 64 + ty * 4 + r % 4;
     if (i >= N) continue;
     float *crow = Cb + i * static_cast<int64_t>(N);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int j = j0 + half * 64 + tx * 4;
+    for (int gi = 0; gi < G; ++gi) {
+      const int j = j0 + gi * 64 + tx * 4;
       float x0, x1, x2, x3;
-      f2_unpack(acc[r][2 * half], x0, x1);
-      f2_unpack(acc[r][2 * half + 1], x2, x3);
+      f2_unpack(acc[r][2 * gi], x0, x1);
+      f2_unpack(acc[r][2 * gi + 1], x2, x3);
       if (vec && j + 3 < N) {
         *reinterpret_cast<float4 *>(crow + j) = make_float4(x0, x1, x2, x3);
       } else {
@@ -807,8 +824,18 @@ cudaError_t run_select(const SelectArgs &a, cudaStream_t st) {
   // steps 5-7: scores (the compensation terms are skipped when beta == 0:
   // they are exact zeros then)
   const int ks = (a.beta == 0.f) ? D : 3 * D;
-  k_scores<<<dim3((N + 127) / 128, (N + 127) / 128, static_cast<unsigned>(bh)), 256, 0, st>>>(
-      aug_q, aug_k, scores, N, ks, 3 * D);
+  // 128-wide tiles unless that grid would leave more than half of the SMs
+  // idle; there the 64-wide tiles (a quarter of the serial work per thread)
+  // finish sooner (L = 8192, B = 64: 0.140 -> 0.134 ms for the selection),
+  // while on a grid of one CTA per SM (L = 32768, B = 128) they lose to
+  // L2 latency per k-chunk (0.377 -> 0.396 ms)
+  const int64_t t128 = static_cast<int64_t>((N + 127) / 128) * ((N + 127) / 128) * bh;
+  if (2 * t128 >= 152)
+    k_scores<128><<<dim3((N + 127) / 128, (N + 127) / 128, static_cast<unsigned>(bh)), 256, 0, st>>>(
+        aug_q, aug_k, scores, N, ks, 3 * D);
+  else
+    k_scores<64><<<dim3((N + 63) / 64, (N + 63) / 64, static_cast<unsigned>(bh)), 256, 0, st>>>(
+        aug_q, aug_k, scores, N, ks, 3 * D);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   // steps 8-11: top-kappa (keys of a row in registers: 32 * KPL >= N)
