@@ -747,14 +747,15 @@ size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool p
 // enough back in launch order (about two waves of CTAs) that a head's rows
 // are complete before its first CTA starts.
 static int gather_lookahead(int npairs) {
-  static int sms = 0;
+  static std::atomic<int> sms_cached{0};
+  int sms = sms_cached.load(std::memory_order_relaxed);
   if (sms == 0) {
     int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      sms = n;
-    else
-      sms = 152;
+    sms = (cudaGetDevice(&dev) == cudaSuccess &&
+           cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+              ? n
+              : 152;
+    sms_cached.store(sms, std::memory_order_relaxed);
   }
   return (2 * sms + npairs - 1) / npairs;
 }
@@ -763,22 +764,20 @@ template <int D, int BK, bool kDense, bool kPack = false>
 static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                const AttnParams &p, int64_t bh, cudaStream_t st) {
   using Lay = AttnLayout<D, BK>;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_attn<D, BK, kDense, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Lay::kAlloc);
-    if (e != cudaSuccess) return e;
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [] {
+    cudaError_t r = cudaFuncSetAttribute(k_attn<D, BK, kDense, kPack>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+    if (r != cudaSuccess) return r;
     // setmaxnreg.inc draws on the registers the block is launched with: a
     // split larger than that pool would never be granted, so refuse it here
     cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, k_attn<D, BK, kDense, kPack>)) != cudaSuccess) return e;
+    if ((r = cudaFuncGetAttributes(&fa, k_attn<D, BK, kDense, kPack>)) != cudaSuccess) return r;
     if (fa.numRegs * kAttnThreads < kSplitRegs(RegSplit<BK>::kLow, RegSplit<BK>::kHigh))
       return cudaErrorInvalidConfiguration;
-    configured_device = dev;
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   const dim3 grid((p.n_tiles + kTiles - 1) / kTiles, static_cast<unsigned>(bh));
   k_attn<D, BK, kDense, kPack><<<grid, kAttnThreads, Lay::kAlloc, st>>>(mq, mk, mv, p);
   return cudaGetLastError();

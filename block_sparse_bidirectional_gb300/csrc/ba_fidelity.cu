@@ -410,15 +410,11 @@ template <int D, int BK>
 static cudaError_t launch_fid_mass(const CUtensorMap &mq, const CUtensorMap &mk, const FidMassParams &p,
                             int64_t bh, cudaStream_t st) {
   using Lay = FidLayout<D, BK>;
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t e = once_per_device(configured, [] {
+    return cudaFuncSetAttribute(k_fid_mass<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
+  });
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_fid_mass<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kAlloc);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   const dim3 grid((p.L + kFidTile - 1) / kFidTile, static_cast<unsigned>(bh));
   k_fid_mass<D, BK><<<grid, kFidThreads, Lay::kAlloc, st>>>(mq, mk, p);
   return cudaGetLastError();

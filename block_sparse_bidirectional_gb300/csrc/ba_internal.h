@@ -5,7 +5,26 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace ba {
+
+// One-time setup per device (a kernel's cudaFuncSetAttribute before its
+// first launch on that device), safe when several host threads launch: a
+// device's bit in `done` is set only after `setup` succeeded; two threads
+// may both run `setup` for the same device, which is harmless because it is
+// idempotent.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<uint64_t> &done, F &&setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  if ((e = setup()) != cudaSuccess) return e;
+  if (bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
 
 struct SelectArgs {
   const void *q, *k;

@@ -699,16 +699,12 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
   for (int w = kChunk; w < g.win; w <<= 1) ++npasses;
   const int chunks = (g.win + kChunk - 1) / kChunk;
   const size_t smem = 2 * spad_size(kChunk) * sizeof(uint64_t);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = once_per_device(configured, [smem] {
+    return cudaFuncSetAttribute(k_chunk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+  });
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_chunk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   // chunk sort: keys -> buf0 (or pi when no merge pass follows)
   k_chunk_sort<<<dim3(chunks, g.nwin, nseq), kSortThreads, smem, st>>>(keys, buf0, perm0, perm1,
                                                                         g, npasses == 0);
@@ -734,16 +730,12 @@ template <int D, int BK>
 static cudaError_t launch_stats(const SelectArgs &a, int64_t bh, int N, float *aug_q, float *aug_k,
                                 cudaStream_t st) {
   const size_t smem = 2 * BK * D * 2 + kStatsBlocksPerCta * BK * sizeof(int);
-  static int configured_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<uint64_t> configured{0};
+  const cudaError_t e = once_per_device(configured, [smem] {
+    return cudaFuncSetAttribute(k_block_stats<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem));
+  });
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(k_block_stats<D, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
   const dim3 grid((N + kStatsBlocksPerCta - 1) / kStatsBlocksPerCta, static_cast<unsigned>(bh), 2);
   k_block_stats<D, BK><<<grid, kStatsThreads, smem, st>>>(
       static_cast<const __nv_bfloat16 *>(a.q), static_cast<const __nv_bfloat16 *>(a.k), a.perm_q,
