@@ -55,7 +55,7 @@ def peaks():
 # DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
 # of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
 # for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
-ATTN_TRAFFIC = {"ultra64k": dict(bytes=5219350016, kernel_sha="1d5a7eae8a15c3f3")}
+ATTN_TRAFFIC = {"ultra64k": dict(bytes=5254583296, kernel_sha="b9e2c88e890a639a")}
 
 
 def attn_traffic(workload: str):
