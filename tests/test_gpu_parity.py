@@ -93,6 +93,16 @@ def test_small_select_and_attention(dev, shape, mode):
     _attn_and_check(q, k, v, B, sel, g, dev)
 
 
+@pytest.mark.parametrize("beta", [0.5, 2.5])
+@pytest.mark.parametrize("shape", [(1, 2, 2048, 128, 128, 6), (1, 2, 1500, 64, 64, 9)])
+def test_beta_scaling(dev, shape, beta):
+    """beta other than 0 and 1 (Eq. 13): scores, mask and attention."""
+    b, h, L, d, B, kappa = shape
+    q, k, v = workloads.random_inputs(b, h, L, d, seed=31 + L + int(10 * beta), scale=1.5)
+    sel, g = _select_and_check(q, k, B, kappa, beta, 3, 0, dev)
+    _attn_and_check(q, k, v, B, sel, g, dev)
+
+
 @pytest.mark.parametrize("window", [128, 512])
 def test_windowed_sort(dev, window):
     q, k, v = workloads.random_inputs(1, 2, 2048 + 128, 128, seed=77, scale=2.0)
