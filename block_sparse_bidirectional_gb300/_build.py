@@ -19,7 +19,8 @@ OUT_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(OUT_DIR, "libba.so")
 BUILD_DIR = os.path.join(OUT_DIR, "obj")
 
-SOURCES = ["ba_api.cu", "ba_select.cu", "ba_attn.cu", "ba_noalloc.cu", "ba_merge.cu", "ba_fidelity.cu", "ba_losa.cu"]
+SOURCES = ["ba_api.cu", "ba_select.cu", "ba_attn.cu", "ba_noalloc.cu", "ba_merge.cu", "ba_fidelity.cu", "ba_losa.cu",
+           "ba_selftest.cu"]
 HEADERS = ["ba_common.cuh", "ba_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -348,13 +348,21 @@ int ba_merge_lse(const void *o1, const float *lse1, const void *o2, const float 
                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return BA_ERR_INVALID_ARG;
+  return map_cuda(run_selftest_wait(static_cast<uint64_t>(limit_us) * 1000ull,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ba_last_device_error(ba_stream_t stream, uint32_t *detail) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BA_ERR_CUDA;
-  uint32_t word = 0, fid = 0;
+  uint32_t word = 0, fid = 0, self = 0;
   if (take_attn_error_word(&word) != cudaSuccess) return BA_ERR_CUDA;
   if (take_fidelity_error_word(&fid) != cudaSuccess) return BA_ERR_CUDA;
+  if (take_selftest_error_word(&self) != cudaSuccess) return BA_ERR_CUDA;
   if (word == 0) word = fid;
+  if (word == 0) word = self;
   if (detail) *detail = word;
   return (word & 1u) ? BA_ERR_DEVICE_TIMEOUT : BA_OK;
 }

@@ -32,6 +32,7 @@ enum WaitSite : uint32_t {
   kSiteODone = 8,
   kSiteDrain = 9,
   kSiteRowsReady = 10,
+  kSiteSelfTest = 11,
 };
 
 // A wait gives up after this many nanoseconds of wall time (2 s).
@@ -90,10 +91,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (after recording the site) when the deadline passes or another role of the
-// CTA has already aborted (*abort != 0).
+// (after recording the site) when the deadline (limit_ns after the first
+// failed test) passes or another role of the CTA has already aborted
+// (*abort != 0).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t site,
-                                          volatile int *abort) {
+                                          volatile int *abort, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   uint32_t spins = 0;
@@ -101,7 +103,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     if (mbar_try_wait(bar, parity)) return true;
     if (((++spins) & 63u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         report_timeout(site);
         *abort = 1;
         return false;

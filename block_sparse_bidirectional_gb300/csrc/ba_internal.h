@@ -76,6 +76,8 @@ struct FidArgs {
 size_t fidelity_workspace_bytes(int64_t bh, int L, int D, int B);
 cudaError_t run_fidelity(const FidArgs &a, cudaStream_t st);
 cudaError_t take_fidelity_error_word(uint32_t *word);
+cudaError_t run_selftest_wait(uint64_t limit_ns, cudaStream_t st);
+cudaError_t take_selftest_error_word(uint32_t *word);
 
 size_t select_workspace_bytes(int64_t bh, int L, int D, int B, int sort_mode);
 cudaError_t run_select(const SelectArgs &a, cudaStream_t st);

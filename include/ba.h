@@ -313,6 +313,20 @@ int ba_merge_lse(const void *o1, const float *lse1, const void *o2,
  */
 int ba_last_device_error(ba_stream_t stream, uint32_t *detail);
 
+/*
+ * ba_selftest_wait_timeout: exercises the bounded-wait failure path that
+ * ba_last_device_error reports, without a GPU fault.  Launches one warp on
+ * `stream` that waits, for at most limit_us microseconds, for a phase of a
+ * barrier on which nothing ever arrives; the wait gives up, records site 11
+ * in the device error word and the kernel returns.  A following
+ * ba_last_device_error() returns BA_ERR_DEVICE_TIMEOUT with detail
+ * (11 << 8) | 1 and clears the word; the context stays usable.
+ *   limit_us   1 .. 1000000; anything else returns BA_ERR_INVALID_ARG and
+ *              launches nothing.
+ * Returns BA_OK, or BA_ERR_CUDA if the launch fails.
+ */
+int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -251,3 +251,9 @@ def test_merge_lse_rejects():
     assert lib.ba_merge_lse(P, P, P, P, 10, 96, P, P, None) == UNSUPPORTED
     assert lib.ba_merge_lse(None, P, P, P, 10, 128, P, P, None) == INVALID
     assert lib.ba_merge_lse(P, P, MIS, P, 10, 64, P, P, None) == INVALID
+
+
+def test_selftest_rejects_limits_outside_range():
+    lib = bsb.load()
+    for bad in (0, 1000001, 2**32 - 1):
+        assert lib.ba_selftest_wait_timeout(bad, None) == INVALID
