@@ -420,6 +420,25 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize(dev)
     iso_ms = e0.elapsed_time(e1) / 5
+
+    # ---- the selection's variants (the pages' ablation axes, Tab. 7) -------
+    # beta = 0 drops the covariance term ("Ours (Sort)", the pages' fastest
+    # operator); the sort modes choose which sequences are norm-sorted
+    def time_select(beta, mode, reps=5):
+        ws_v = torch.empty(bsb.select_workspace_size(b, h, L, d, B, kappa, mode, 0), dtype=torch.uint8,
+                           device=dev)
+        bsb.ba_select_into(qd, kd, B, kappa, beta, mode, 0, perm_q, perm_k, idx, mask, None, ws_v)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            bsb.ba_select_into(qd, kd, B, kappa, beta, mode, 0, perm_q, perm_k, idx, mask, None, ws_v)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return round(e0.elapsed_time(e1) / reps, 4)
+    variant_ms = dict(select_ms_beta0_sort_qk=time_select(0.0, 3),
+                      select_ms_beta1_sort_k=time_select(1.0, 1),
+                      select_ms_beta1_sort_q=time_select(1.0, 2),
+                      select_ms_beta1_no_sort=time_select(1.0, 0))
     del idx_iso, ws_iso
 
     # ---- end to end through the public API from pinned host memory ----------
@@ -565,6 +584,7 @@ def main():
             step_frac_tensor_burst=round(attn_flops / (ms_step * 1e-3) / 1e12 / pk["bf16"], 4),
             pages_speedup_context=PAGES_SPEEDUP,
             isolated_select_ms=round(iso_ms, 4),
+            **variant_ms,
             active_tokens_ms=round(losa_ms, 4),
             active_tokens_gbs=round(losa_bytes / (losa_ms * 1e-3) / 1e9, 1),
             active_tokens_frac_hbm_measured=round(losa_bytes / (losa_ms * 1e-3) / 1e9 / peaks()["hbm"], 4),
