@@ -23,7 +23,7 @@ __all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_
            "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into", "ba_block_fidelity",
            "ba_active_tokens", "ba_reuse_rows",
            "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
-           "last_device_error", "selftest_wait_timeout", "BAError",
+           "last_device_error", "selftest_wait_timeout", "selftest_attn_stall", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
            "sparse_attn_workspace_size", "header_functions", "LIB_PATH"]
 
@@ -46,6 +46,7 @@ _SIGS = {
     "ba_attn_dense": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [_c_float] + [_c_void_p] * 3),
     "ba_last_device_error": (_c_int, [_c_void_p, _c_u32p]),
     "ba_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _c_void_p]),
+    "ba_selftest_attn_stall": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [ctypes.c_uint32] + [_c_void_p] * 3),
     "ba_merge_lse": (_c_int, [_c_void_p] * 4 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
     "ba_select_isolated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 8 + [_c_float, _c_int, _c_int]
                            + [_c_void_p] * 6 + [_c_size, _c_void_p]),
@@ -361,6 +362,18 @@ def selftest_wait_timeout(limit_us=1000, device=None):
     lib = load()
     _check(lib.ba_selftest_wait_timeout(int(limit_us), _stream(device or torch.device("cuda"))),
            "ba_selftest_wait_timeout")
+
+
+def selftest_attn_stall(q, k, v, o, lse, limit_us=1000):
+    """Run the dense attention kernel with its second K/V stage never loaded,
+    so that the MMA thread's bounded wait runs out after ``limit_us`` and the
+    kernel unwinds (no fault, nothing written to o / lse); read the result
+    with last_device_error()."""
+    lib = load()
+    _need_cuda(q, k, v, o, lse)
+    b, h, L, d = q.shape
+    _check(lib.ba_selftest_attn_stall(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, int(limit_us), _ptr(o),
+                                      _ptr(lse), _stream(q.device)), "ba_selftest_attn_stall")
 
 
 def last_device_error(device=None):

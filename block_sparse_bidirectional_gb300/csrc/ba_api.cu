@@ -354,6 +354,33 @@ int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream) {
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ba_selftest_attn_stall(const void *q, const void *k, const void *v, int batch, int heads,
+                           int seqlen, int head_dim, uint32_t limit_us, void *o, float *lse,
+                           ba_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return BA_ERR_INVALID_ARG;
+  int st = check_shape(batch, heads, seqlen, head_dim, 128);
+  if (st != BA_OK) return st;
+  // stage 1 must exist: at least two 128-key slots
+  if (seqlen <= 128) return BA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return BA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return BA_ERR_INVALID_ARG;
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.batch = batch;
+  a.heads = heads;
+  a.seqlen = seqlen;
+  a.head_dim = head_dim;
+  a.block = 128;
+  a.o = o;
+  a.lse = lse;
+  return map_cuda(run_attention_stall(a, static_cast<uint64_t>(limit_us) * 1000ull,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int ba_last_device_error(ba_stream_t stream, uint32_t *detail) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return BA_ERR_CUDA;

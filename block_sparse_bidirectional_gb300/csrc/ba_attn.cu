@@ -108,22 +108,28 @@ struct AttnParams {
   const uint16_t *pair_lists;  // [b*h][npairs][2][N]: per tile, common blocks first
   const int32_t *pair_counts;  // [b*h][npairs][4]: n0, n1, common, -
   const int32_t *perm_q;  // sorted query position -> original row (nullable)
-  // Row gathers done inside the kernel by warps 2-3: CTA `pair` of head bh
-  // writes rows [pair * slice_rows, +slice_rows) of Q', K', V' of head
-  // bh + lookahead, then counts itself in ready[bh + lookahead].  CTAs of a
-  // head >= lookahead wait for ready[head] == npairs before their first TMA
-  // load; heads < lookahead were gathered by a kernel launched before.
-  // ready == nullptr: no in-kernel gathers, no waits.
+  // Row gathers inside the kernel by warps 2-3 (claim != nullptr): head h's
+  // rows are cut into nslices slices of slice_rows rows.  A slice is claimed
+  // with an atomic ticket on claim[h] and counted in done[h] once written.
+  // CTAs of head h - lookahead each claim one slice ahead of time, and CTAs
+  // of head h claim every slice still unclaimed when they start, so a CTA
+  // waits only on slices that running CTAs hold, whatever order the CTAs
+  // are dispatched in.  Heads < lookahead were gathered by a kernel launched
+  // before.
   const int32_t *perm_k;
   const __nv_bfloat16 *src_q, *src_k, *src_v;  // unpermuted inputs
   __nv_bfloat16 *dst_q, *dst_k, *dst_v;        // Q' (or null), K' and V' (or null)
-  int *ready;
+  int *claim;
+  int *done;
   int lookahead;
   int bh_total;
   int slice_rows;
+  int nslices;
   __nv_bfloat16 *o;
   float *lse;
-  float scale_log2;       // scale * log2(e)
+  float scale_log2;          // scale * log2(e)
+  uint64_t issuer_wait_ns;   // wait limit of the MMA thread (the other roles: 2 s)
+  int skip_load;             // failure-path test only: this K/V load is never issued; -1 otherwise
 };
 
 // A key-block entry: bits 0-11 block id, bit 12+g set when query block g of
@@ -167,6 +173,28 @@ __device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pa
   }
 }
 
+// Named barrier of the two gather warps (id 0 is __syncthreads).
+__device__ __forceinline__ void gather_bar() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+
+// One ticket from `counter`, broadcast to the 64 gather threads.
+__device__ __forceinline__ int claim_slice(int *counter, volatile int *bcast, int tid) {
+  if (tid == 0) *bcast = atomicAdd(counter, 1);
+  gather_bar();
+  const int s = *bcast;
+  gather_bar();  // every thread has read it before the next ticket overwrites it
+  return s;
+}
+
+// Publish a written slice: after the barrier, one thread orders every gather
+// thread's stores before its count (fence cumulativity) and counts the slice.
+__device__ __forceinline__ void publish_slice(int *done, int tid) {
+  gather_bar();
+  if (tid == 0) {
+    __threadfence();
+    atomicAdd(done, 1);
+  }
+}
+
 template <int D, int BK, bool kDense, bool kPack>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     k_attn(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -186,7 +214,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint64_t *p_full = s_full + kTiles;  // [kTiles]
   uint64_t *o_done = p_full + kTiles;  // [kTiles]
   uint64_t *drain = o_done + kTiles;
-  uint32_t *misc = reinterpret_cast<uint32_t *>(drain + 1);  // tmem, n0, n1, abort, common
+  uint32_t *misc = reinterpret_cast<uint32_t *>(drain + 1);  // tmem, n0, n1, abort, common, ticket
   volatile int *abort_flag = reinterpret_cast<volatile int *>(&misc[3]);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -250,10 +278,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      // this head's Q', K', V' rows come from CTAs of an earlier head; on a
-      // timeout the error word is set and the loads go ahead regardless
-      if (p.ready != nullptr && bh >= p.lookahead)
-        wait_counter_at_least(p.ready + bh, p.npairs, kSiteRowsReady);
+      // this head's Q', K', V' rows: every slice is held by a running CTA; a
+      // wait that runs out aborts the CTA before any load (nothing is
+      // computed from rows that were not written)
+      bool rows_ok = true;
+      if (p.claim != nullptr && bh >= p.lookahead) {
+        rows_ok = wait_counter_at_least(p.done + bh, p.nslices, kSiteRowsReady);
+        if (!rows_ok) *abort_flag = 1;
+      }
+      uint32_t loaded = 0u, parity = 0u;  // per ring slot: ever loaded, parity of its loads
+      if (rows_ok) {
       uint32_t qbytes = 0;
       for (int t = 0; t < kTiles; ++t) qbytes += n_t[t] > 0 ? Lay::kQBytes : 0;
       mbar_arrive_expect_tx(q_full, qbytes);
@@ -276,7 +310,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int s = issued % S;
         if (issued >= S && !mbar_wait(&slot_empty[s], ((issued / S) & 1) ^ 1u, kSiteKEmpty, abort_flag))
           return false;
+        if (issued == p.skip_load) {  // failure-path test: this copy never happens
+          ++issued;
+          return true;
+        }
         mbar_arrive_expect_tx(&slot_full[s], Lay::kSlotBytes);
+        loaded |= 1u << s;
+        parity ^= 1u << s;
         const CUtensorMap *map = is_v ? &tmV : &tmK;
         uint8_t *dst = sSlot + s * Lay::kSlotBytes;
 #pragma unroll
@@ -305,21 +345,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
       // drain: the last copy issued into each slot has landed
       mbar_wait_drain(q_full, 0);
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int last = s + S * ((issued - 1 - s) / S);
-        mbar_wait_drain(&slot_full[s], (last / S) & 1);
       }
+      for (int s = 0; s < S; ++s)
+        if ((loaded >> s) & 1u) mbar_wait_drain(&slot_full[s], ((parity >> s) & 1u) ^ 1u);
     } else if (warp == 1 && lane == 0) {
       // ===================== MMA issuer =====================================
       const uint32_t idS = idesc_bf16_f32(kTileM, BK, 0, 0);
       const uint32_t idO = idesc_bf16_f32(kTileM, D, 0, 1);
       const uint32_t q_addr = smem_u32(sQ), slot_addr = smem_u32(sSlot);
       int consumed = 0;
-      bool ok = mbar_wait(q_full, 0, kSiteQFull, abort_flag);
+      const uint64_t lim = p.issuer_wait_ns;
+      bool ok = mbar_wait(q_full, 0, kSiteQFull, abort_flag, lim);
       tc_fence_after();
       auto take = [&](int &slot) -> bool {
         slot = consumed % S;
-        if (!mbar_wait(&slot_full[slot], (consumed / S) & 1, kSiteKFull, abort_flag)) return false;
+        if (!mbar_wait(&slot_full[slot], (consumed / S) & 1, kSiteKFull, abort_flag, lim)) return false;
         tc_fence_after();
         ++consumed;
         return true;
@@ -357,7 +397,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       for (int j = 0; ok && j < nmax; ++j) {
         for (int t = 0; ok && t < kTiles; ++t) {
           if (j >= n_t[t]) continue;
-          if (!(ok = mbar_wait(&p_full[t], j & 1, kSitePFull, abort_flag))) break;
+          if (!(ok = mbar_wait(&p_full[t], j & 1, kSitePFull, abort_flag, lim))) break;
           tc_fence_after();
           const bool shv = j < n_common;
           int sv = slot_v0;
@@ -378,15 +418,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
-    } else if (warp >= 2 && p.ready != nullptr) {
-      // ===================== row gathers for a later head ===================
+    } else if (warp >= 2 && p.claim != nullptr) {
+      // ===================== row gathers ====================================
+      const int tid = threadIdx.x - 64;
+      volatile int *bcast = reinterpret_cast<volatile int *>(&misc[5]);
+      if (bh >= p.lookahead) {
+        // slices of this CTA's own head that nobody has claimed yet
+        for (;;) {
+          const int s = claim_slice(p.claim + bh, bcast, tid);
+          if (s >= p.nslices) break;
+          gather_slice<D>(p, bh, s, tid);
+          publish_slice(p.done + bh, tid);
+        }
+      }
+      // one slice of a later head, ahead of time
       const int hp = bh + p.lookahead;
       if (hp < p.bh_total) {
-        gather_slice<D>(p, hp, pair, threadIdx.x - 64);
-        asm volatile("bar.sync 1, 64;" ::: "memory");
-        if (threadIdx.x == 64) {
-          __threadfence();
-          atomicAdd(p.ready + hp, 1);
+        const int s = claim_slice(p.claim + hp, bcast, tid);
+        if (s < p.nslices) {
+          gather_slice<D>(p, hp, s, tid);
+          publish_slice(p.done + hp, tid);
         }
       }
     }
@@ -544,8 +595,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float la, lb;
       f2_unpack(l2, la, lb);
       const float l = la + lb;
+      // (an out-of-range permutation entry is clamped: wrong rows, never a
+      // write outside this head's output)
       const int64_t orig =
-          row_valid ? (p.perm_q ? p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted] : row_sorted)
+          row_valid ? (p.perm_q ? min(max(p.perm_q[static_cast<int64_t>(bh) * p.L + row_sorted], 0), p.L - 1)
+                                : row_sorted)
                     : 0;
       const float lo = l + lcorr;
       const float inv = (lo > 0.f) ? 1.f / lo : 0.f;
@@ -638,7 +692,7 @@ __global__ void __launch_bounds__(kPairWarps * 32) k_pair_lists(
   __shared__ uint32_t bm[kPairWarps][kTiles][G][kPairWords];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   {
-    // the attention kernel's per-head gather counters start from zero
+    // the attention kernel's per-head gather counters (claim, done) start from zero
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (ready != nullptr && i < n_ready) ready[i] = 0;
   }
@@ -729,7 +783,8 @@ cudaError_t take_attn_error_word(uint32_t *word) {
 }
 
 // Workspace of the sparse call: Q' (perm_q), K' and V' (perm_k), then the
-// tile-pair lists and their counts.
+// tile-pair lists and their counts, then (with a permutation) the gather
+// claim and done counters, one of each per head.
 static size_t pair_list_bytes(int64_t bh, int L, int B) {
   const int64_t n = (L + B - 1) / B;
   const int64_t npairs = ((L + kTileM - 1) / kTileM + kTiles - 1) / kTiles;
@@ -739,23 +794,23 @@ static size_t pair_list_bytes(int64_t bh, int L, int B) {
 
 size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool perm_k) {
   const size_t t = align256(static_cast<size_t>(bh) * L * D * 2);
-  const size_t ready = (perm_q || perm_k) ? align256(static_cast<size_t>(bh) * sizeof(int)) : 0;
-  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0) + pair_list_bytes(bh, L, B) + ready;
+  const size_t counters = (perm_q || perm_k) ? align256(static_cast<size_t>(2 * bh) * sizeof(int)) : 0;
+  return (perm_q ? t : 0) + (perm_k ? 2 * t : 0) + pair_list_bytes(bh, L, B) + counters;
 }
 
 // Heads between an attention CTA and the head whose rows it gathers: far
 // enough back in launch order (about two waves of CTAs) that a head's rows
 // are complete before its first CTA starts.
 static int gather_lookahead(int npairs) {
-  static std::atomic<int> sms_cached{0};
-  int sms = sms_cached.load(std::memory_order_relaxed);
+  static std::atomic<int> sms_cached[64];  // per device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
+  std::atomic<int> &slot = sms_cached[dev & 63];
+  int sms = slot.load(std::memory_order_relaxed);
   if (sms == 0) {
-    int dev = 0, n = 0;
-    sms = (cudaGetDevice(&dev) == cudaSuccess &&
-           cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-              ? n
-              : 152;
-    sms_cached.store(sms, std::memory_order_relaxed);
+    int n = 0;
+    sms = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) ? n : 152;
+    slot.store(sms, std::memory_order_relaxed);
   }
   return (2 * sms + npairs - 1) / npairs;
 }
@@ -783,7 +838,8 @@ static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, con
   return cudaGetLastError();
 }
 
-cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
+static cudaError_t run_attention_impl(const AttnArgs &a, cudaStream_t st, uint64_t issuer_wait_ns,
+                                      int skip_load) {
   const int64_t bh = static_cast<int64_t>(a.batch) * a.heads;
   const int L = a.seqlen, D = a.head_dim;
   const bool dense = a.block_idx == nullptr;
@@ -821,8 +877,8 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   const int n_tiles = (L + kTileM - 1) / kTileM;
   const int npairs = (n_tiles + kTiles - 1) / kTiles;
   // Gathers: the first `lookahead` heads by k_gather_rows before the
-  // attention kernel, the others by the attention CTAs of earlier heads.
-  int *ready = nullptr;
+  // attention kernel, the others inside it (claimed slices).
+  int *counters = nullptr;
   const int lookahead = gather_lookahead(npairs);
   const bool in_kernel_gathers = !dense && njobs > 0 && lookahead < bh;
   if (!dense) {
@@ -830,18 +886,20 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
     pair_lists = reinterpret_cast<uint16_t *>(ws);
     const size_t list_bytes = align256(static_cast<size_t>(bh * npairs * kTiles * nblk) * sizeof(uint16_t));
     pair_counts = reinterpret_cast<int32_t *>(ws + list_bytes);
-    if (in_kernel_gathers) ready = reinterpret_cast<int *>(ws + pair_list_bytes(bh, L, BK));
+    if (in_kernel_gathers) counters = reinterpret_cast<int *>(ws + pair_list_bytes(bh, L, BK));
     const int64_t total = bh * npairs;
-    const unsigned grid = static_cast<unsigned>((total + kPairWarps - 1) / kPairWarps);
-    const int n_ready = ready ? static_cast<int>(bh) : 0;
+    const int n_ready = counters ? static_cast<int>(2 * bh) : 0;
+    const int64_t by_pairs = (total + kPairWarps - 1) / kPairWarps;
+    const int64_t by_counters = (n_ready + kPairWarps * 32 - 1) / (kPairWarps * 32);
+    const unsigned grid = static_cast<unsigned>(by_pairs > by_counters ? by_pairs : by_counters);
     if (BK == 128)
       k_pair_lists<1><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
                                                         n_tiles, npairs, total, pair_lists, pair_counts,
-                                                        ready, n_ready);
+                                                        counters, n_ready);
     else
       k_pair_lists<2><<<grid, kPairWarps * 32, 0, st>>>(a.block_idx, static_cast<int>(nblk), a.kappa,
                                                         n_tiles, npairs, total, pair_lists, pair_counts,
-                                                        ready, n_ready);
+                                                        counters, n_ready);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (njobs > 0) {
@@ -875,10 +933,14 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
   p.dst_q = a.perm_q ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(qs)) : nullptr;
   p.dst_k = a.perm_k ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(ks)) : nullptr;
   p.dst_v = a.perm_k ? const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(vs)) : nullptr;
-  p.ready = ready;
+  p.claim = counters;
+  p.done = counters ? counters + bh : nullptr;
   p.lookahead = lookahead;
   p.bh_total = static_cast<int>(bh);
   p.slice_rows = (L + npairs - 1) / npairs;
+  p.nslices = npairs;
+  p.issuer_wait_ns = issuer_wait_ns;
+  p.skip_load = skip_load;
   p.o = static_cast<__nv_bfloat16 *>(a.o);
   p.lse = a.lse;
   const float scale = (a.scale > 0.f) ? a.scale : 1.0f / sqrtf(static_cast<float>(D));
@@ -894,6 +956,18 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
     if (D == 64 && BK == 64) return launch_attn<64, 128, false, true>(mq, mk, mv, p, bh, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
+  return run_attention_impl(a, st, kWaitLimitNs, -1);
+}
+
+// The dense kernel with the second K/V copy of every CTA (V_0) never issued:
+// the MMA thread's bounded wait for it gives up after `limit_ns` and records
+// kSiteKFull; every role unwinds (copies and MMAs drained, tensor memory
+// freed, nothing written).
+cudaError_t run_attention_stall(const AttnArgs &a, uint64_t limit_ns, cudaStream_t st) {
+  return run_attention_impl(a, st, limit_ns, 1);
 }
 
 }  // namespace ba

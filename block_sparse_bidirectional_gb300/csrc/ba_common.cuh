@@ -140,14 +140,15 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
 // scope, then orders the data those writers published before this thread's
 // later TMA (async-proxy) reads of global memory.  On a timeout the site is
 // recorded and the wait returns false.
-__device__ __forceinline__ bool wait_counter_at_least(const int *counter, int target, uint32_t site) {
+__device__ __forceinline__ bool wait_counter_at_least(const int *counter, int target, uint32_t site,
+                                                      uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = global_ns();
   bool ok = true;
   for (;;) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
     if (v >= target) break;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       report_timeout(site);
       ok = false;
       break;
@@ -218,6 +219,65 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= 1ull << 46;  // descriptor version for tcgen05
   d |= 2ull << 61;  // 128-byte swizzle
   return d;
+}
+
+// The same descriptor as two 32-bit words.  The low word holds the start
+// address (bits 0-13, 16-byte units) and the leading byte offset (bits
+// 16-29); the high word holds the stride byte offset, the version and the
+// swizzle mode, constant per operand.  A byte offset (a multiple of 16 that
+// keeps the address inside the 256 KB window) added to the address adds
+// offset / 16 to the low word, so an issuing loop needs one add per operand.
+__host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+
+// tcgen05.mma kind::f16 with both operands in shared memory, descriptors
+// given as (low, high) words; kPair selects cta_group::2 (issued by rank 0
+// of the CTA pair: M = 256, each CTA holding half of A's rows and of B's).
+template <bool kPair>
+__device__ __forceinline__ void mma_ss_words(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                             uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kPair) {
+    asm volatile(
+        "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\t"
+        "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .b64 da, db;\n\t.reg .pred p;\n\t"
+        "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+// tcgen05.mma kind::f16 with A in tensor memory and B in shared memory.
+template <bool kPair>
+__device__ __forceinline__ void mma_ts_words(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                             uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kPair) {
+    asm volatile(
+        "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\t"
+        "mov.b64 db, {%2, %3};\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .b64 db;\n\t.reg .pred p;\n\t"
+        "mov.b64 db, {%2, %3};\n\tsetp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.

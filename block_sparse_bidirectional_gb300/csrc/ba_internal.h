@@ -84,6 +84,9 @@ cudaError_t run_select(const SelectArgs &a, cudaStream_t st);
 
 size_t attn_workspace_bytes(int64_t bh, int L, int D, int B, bool perm_q, bool perm_k);
 cudaError_t run_attention(const AttnArgs &a, cudaStream_t st);
+// Dense attention whose second K/V stage is never loaded: exercises the
+// attention kernel's bounded-wait unwind (see ba_selftest_attn_stall).
+cudaError_t run_attention_stall(const AttnArgs &a, uint64_t limit_ns, cudaStream_t st);
 
 cudaError_t run_merge_lse(const void *o1, const float *lse1, const void *o2, const float *lse2,
                           int64_t rows, int head_dim, void *o, float *lse, cudaStream_t st);

@@ -327,6 +327,27 @@ int ba_last_device_error(ba_stream_t stream, uint32_t *detail);
  */
 int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream);
 
+/*
+ * ba_selftest_attn_stall: exercises the attention kernel's own failure path
+ * (BA-Att paper Algorithm 1 step 12 is the kernel under test) without a GPU
+ * fault.  Runs ba_attn_dense on the caller's buffers with one change: the
+ * second K/V copy of every CTA (the first V block) is never issued, so the
+ * MMA-issuing thread's bounded wait for it runs out after limit_us
+ * microseconds and records site 2 in the device error word.  Every role of
+ * the CTA then unwinds: the copies and MMAs it issued complete, its tensor
+ * memory is freed, and no O or LSE element is written.  A following
+ * ba_last_device_error() returns BA_ERR_DEVICE_TIMEOUT with detail
+ * (2 << 8) | 1 and clears the word; the context stays usable.
+ *   q, k, v, o, lse, shape: as in ba_attn_dense; seqlen must exceed 128 (two
+ *              key blocks), else BA_ERR_INVALID_ARG.
+ *   limit_us   1 .. 1000000, else BA_ERR_INVALID_ARG.
+ * Every CTA waits limit_us, in waves of one CTA per SM: keep the shape small.
+ */
+int ba_selftest_attn_stall(const void *q, const void *k, const void *v,
+                           int batch, int heads, int seqlen, int head_dim,
+                           uint32_t limit_us, void *o, float *lse,
+                           ba_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,8 +57,8 @@ def test_workspace_sizes():
     # tile-pair lists (uint16, two tiles of N entries per CTA) and their counts
     npairs = ((L + 127) // 128 + 1) // 2
     pl = a256(b * h * npairs * 2 * N * 2) + a256(b * h * npairs * 4 * 4)
-    # with a permutation: the permuted copies and one gather counter per head
-    rc = a256(b * h * 4)
+    # with a permutation: the permuted copies and two gather counters per head
+    rc = a256(b * h * 2 * 4)
     assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 1, 1) == 3 * t + pl + rc
     assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 1) == 2 * t + pl + rc
     assert lib.ba_sparse_attn_workspace_size(b, h, L, d, B, 256, 0, 0) == pl

@@ -47,3 +47,36 @@ def test_context_usable_after_a_timeout(dev):
     o_ref, lse_ref = O.sparse_attention(to64(q), to64(k), to64(v), g["perm_q"], g["perm_k"],
                                         g["block_idx"], 128)
     check_attention(to64(o), lse.cpu().double().numpy(), o_ref, lse_ref)
+
+
+SITE_K_FULL = 2  # the MMA thread's wait for a K/V copy that is never issued
+
+
+def test_attention_kernel_unwinds_after_a_stalled_stage(dev):
+    """The attention kernel's own bounded wait runs out (its MMA thread waits
+    for a K/V copy that is never issued): the site is reported, nothing is
+    written, the word clears, and the next select + attention matches the
+    oracle."""
+    assert bsb.last_device_error() == (0, 0)
+    q, k, v = workloads.random_inputs(1, 2, 1024, 128, seed=5)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, 7.0)
+    lse = torch.full((1, 2, 1024), 7.0, dtype=torch.float32, device=dev)
+    bsb.selftest_attn_stall(qd, kd, vd, o, lse, limit_us=1000)
+    st, word = bsb.last_device_error()
+    assert st == DEVICE_TIMEOUT
+    assert word & 1 and (word >> 8) & 0xFF == SITE_K_FULL
+    assert bsb.last_device_error() == (0, 0)
+    # an aborted CTA writes no output
+    assert bool((o == 7.0).all()) and bool((lse == 7.0).all())
+    sel = bsb.ba_select(qd, kd, 128, 4, 1.0, bsb.SORT_QK)
+    o2, lse2 = bsb.ba_sparse_attn(qd, kd, vd, 128, sel["perm_q"], sel["perm_k"], sel["block_idx"])
+    od, lsed = bsb.ba_attn_dense(qd, kd, vd)
+    torch.cuda.synchronize()
+    assert bsb.last_device_error() == (0, 0)
+    g = {n: t.cpu().numpy() for n, t in sel.items()}
+    o_ref, lse_ref = O.sparse_attention(to64(q), to64(k), to64(v), g["perm_q"], g["perm_k"],
+                                        g["block_idx"], 128)
+    check_attention(to64(o2), lse2.cpu().double().numpy(), o_ref, lse_ref)
+    od_ref, ld_ref = O.dense_attention(to64(q), to64(k), to64(v))
+    check_attention(to64(od), lsed.cpu().double().numpy(), od_ref, ld_ref)
