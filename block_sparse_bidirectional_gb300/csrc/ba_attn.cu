@@ -364,25 +364,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         ++consumed;
         return true;
       };
+      // K-major Q and K (stride 1024 between 8-row groups), MN-major V
+      // (leading offset = one 64-column chunk of a slot): each MMA adds a
+      // constant to a precomputed low descriptor word, one add per operand on
+      // the issuing thread's path instead of a full encoding
+      constexpr uint32_t kHi = desc_sw128_hi(1024);
+      const uint32_t q_lo = desc_sw128_lo(q_addr, 16);
+      const uint32_t k_lo = desc_sw128_lo(slot_addr, 16);
+      const uint32_t v_lo = desc_sw128_lo(slot_addr, BK * 128);
       auto mma_s = [&](int t, int slot) {
-        const uint32_t qa = q_addr + t * Lay::kQBytes;
-        const uint32_t ka = slot_addr + slot * Lay::kSlotBytes;
+        const uint32_t a0 = q_lo + ((t * Lay::kQBytes) >> 4);
+        const uint32_t b0 = k_lo + ((slot * Lay::kSlotBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t a = smem_desc_sw128(qa + (ks / 4) * kTileM * 128 + (ks % 4) * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(ka + (ks / 4) * BK * 128 + (ks % 4) * 32, 16, 1024);
-          mma_bf16_ss(tmem + t * BK, a, b, idS, ks > 0 ? 1u : 0u);
+          const uint32_t oa = ((ks / 4) * kTileM * 128 + (ks % 4) * 32) >> 4;
+          const uint32_t ob = ((ks / 4) * BK * 128 + (ks % 4) * 32) >> 4;
+          mma_ss_words<false>(tmem + t * BK, a0 + oa, b0 + ob, kHi, idS, ks > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[t]);
       };
       auto mma_pv = [&](int t, int slot, int j) {
-        const uint32_t va = slot_addr + slot * Lay::kSlotBytes;
+        const uint32_t b0 = v_lo + ((slot * Lay::kSlotBytes) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint64_t b = smem_desc_sw128(va + ks * 16 * 128, BK * 128, 1024);
-          mma_bf16_ts(tmem + kTiles * BK + t * D, tmem + t * BK + ks * 8, b, idO,
-                      (j > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BK / 16; ++ks)
+          mma_ts_words<false>(tmem + kTiles * BK + t * D, tmem + t * BK + ks * 8, b0 + ((ks * 16 * 128) >> 4), kHi,
+                              idO, (j > 0 || ks > 0) ? 1u : 0u);
       };
       int slot_k0 = 0, slot_v0 = 0;  // shared positions: slots loaded for tile 0, reused by tile 1
       for (int t = 0; ok && t < kTiles; ++t) {
