@@ -52,9 +52,9 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
-# DRAM bytes (read + write) of one attention-kernel launch from an ncu capture
-# of the headline workload (profiles/k_attn_ultra64k_traffic.md), valid only
-# for the kernel source it was taken on (sha256 prefix of csrc/ba_attn.cu).
+# DRAM bytes (read + write) of one attention-kernel launch from the ncu
+# traffic capture of the headline workload, valid only for the kernel source
+# it was taken on (sha256 prefix of csrc/ba_attn.cu).
 ATTN_TRAFFIC = {"ultra64k": dict(bytes=5254583296, kernel_sha="b9e2c88e890a639a")}
 
 
@@ -105,14 +105,14 @@ def dense_flops(w):
     return 4.0 * w.batch * w.heads * w.seqlen * w.seqlen * w.head_dim
 
 
-def select_bytes(w, sort_q=True, sort_k=True):
+def select_bytes(w, sort_q=True, sort_k=True, kappa=None):
     """Algorithmic bytes of the selection stage: Q and K are streamed once for
     the norms of each sorted tensor and once for the block statistics; small
     outputs (pi, index list, mask) are added."""
     t = w.batch * w.heads * w.seqlen * w.head_dim * 2
     reads = (2 if sort_q else 1) * t + (2 if sort_k else 1) * t
     N = w.nblocks
-    kappa = w.kappa()
+    kappa = w.kappa() if kappa is None else kappa
     writes = (2 * w.batch * w.heads * w.seqlen * 4
               + w.batch * w.heads * N * (kappa * 4 + ((N + 31) // 32) * 4))
     return reads + writes
@@ -188,14 +188,14 @@ class ClockSampler:
                     reasons=sorted(reasons), samples=len(sm))
 
 
-def cpu_oracle_sample(w, q, k, v, budget_s=12.0, seed=0):
+def cpu_oracle_sample(w, q, k, v, budget_s=12.0, seed=0, kappa=None):
     """Times the fp64 oracle on one head: its whole selection plus as many
     sampled query blocks of attention as fit in ``budget_s``; extrapolates
     to the head's full work and returns dense-equivalent TFLOPS."""
     import numpy as np
 
     import oracle.ba_oracle as O
-    kappa = w.kappa()
+    kappa = w.kappa() if kappa is None else kappa
     Q = q[0, 0].double().numpy()
     K = k[0, 0].double().numpy()
     V = v[0, 0].double().numpy()
@@ -214,11 +214,59 @@ def cpu_oracle_sample(w, q, k, v, budget_s=12.0, seed=0):
     per_head = t_sel + t_att / done * w.nblocks
     head_flops = 4.0 * w.seqlen * w.seqlen * w.head_dim
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    full = done == w.nblocks and w.heads * w.batch == 1
     return dict(value=head_flops / per_head / 1e12, unit=UNIT, cores=cores, kind="oracle",
                 sample=(f"1 of {w.heads} heads: full selection ({t_sel:.2f} s) + {done} of "
-                        f"{w.nblocks} query blocks of attention ({t_att:.2f} s), extrapolated "
-                        f"linearly to the head ({per_head:.1f} s); fp64 numpy"),
+                        f"{w.nblocks} query blocks of attention ({t_att:.2f} s), "
+                        + ("the whole workload" if full else
+                           f"extrapolated linearly to the head ({per_head:.1f} s) and the {w.heads} heads")
+                        + "; fp64 numpy"),
+                ms_per_step=per_head * w.heads * w.batch * 1e3, extrapolated=not full,
                 seconds=t_sel + t_att)
+
+
+def _oracle_head(job):
+    """One head through the fp64 oracle: selection, then attention over every
+    query block (a process-pool task)."""
+    import numpy as np
+
+    import oracle.ba_oracle as O
+    Q, K, V, B, kappa = job
+    t0 = time.perf_counter()
+    sel = O.select_one(Q, K, B, kappa, 1.0, O.SORT_QK)
+    O.sparse_attention_one(Q, K, V, sel["perm_q"], sel["perm_k"], sel["idx"], B,
+                           query_blocks=list(range(-(-Q.shape[0] // B))))
+    return time.perf_counter() - t0
+
+
+def cpu_oracle_full(w, q, k, v, kappa, workers=None):
+    """The fp64 oracle over the whole workload (every head, every query
+    block), one head per task on a spawn-started process pool."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    workers = max(1, min(workers or cores, w.batch * w.heads))
+    jobs = [(q[bb, hh].double().numpy(), k[bb, hh].double().numpy(), v[bb, hh].double().numpy(), w.block, kappa)
+            for bb in range(w.batch) for hh in range(w.heads)]
+    # one BLAS thread per worker process (the workers inherit the environment
+    # when they are spawned; the parent's own BLAS is already set up)
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {key: os.environ.get(key) for key in keys}
+    os.environ.update({key: "1" for key in keys})
+    try:
+        t0 = time.perf_counter()
+        with mp.get_context("spawn").Pool(workers) as pool:
+            per_head = pool.map(_oracle_head, jobs, chunksize=1)
+        wall = time.perf_counter() - t0
+    finally:
+        for key, val in saved.items():
+            if val is None:
+                os.environ.pop(key, None)
+            else:
+                os.environ[key] = val
+    return dict(ms_per_step=wall * 1e3, extrapolated=False, cores=workers,
+                sample=(f"the whole workload: {len(jobs)} heads, selection + attention over every query block, "
+                        f"one head per task on {workers} spawned processes (wall {wall:.1f} s, sum of head "
+                        f"times {sum(per_head):.1f} s, pool start-up included); fp64 numpy"))
 
 
 def run_reference(args):
@@ -257,6 +305,89 @@ def workload_config(w):
                 parallelism="independent heads per GPU (no collective)")
 
 
+def measure_workload(bsb, w, sparsity, dev, steps=5, dense_steps=2, cpu_budget_s=4.0, with_cpu=True):
+    """One workload at one sparsity, as its own select + sparse attention
+    step: stage times (CUDA events, median of ``steps``), attention TFLOP/s on
+    the computed tiles and its fraction of the bf16 peak, selection GB/s,
+    the library's dense kernel at the same shape, and a bounded sample of the
+    fp64 oracle on the host cores."""
+    import numpy as np
+    import torch
+
+    import workloads
+    q, k, v, _ = workloads.make_inputs(w)
+    kappa = w.kappa(sparsity)
+    b, h, L, d, B, N = w.batch, w.heads, w.seqlen, w.head_dim, w.block, w.nblocks
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    perm_q, perm_k = torch.empty((b, h, L), **i32), torch.empty((b, h, L), **i32)
+    idx = torch.empty((b, h, N, kappa), **i32)
+    mask = torch.empty((b, h, N, (N + 31) // 32), **i32)
+    ws_sel = torch.empty(bsb.select_workspace_size(b, h, L, d, B, kappa, 3, 0), dtype=torch.uint8, device=dev)
+    ws_att = torch.empty(max(1, bsb.sparse_attn_workspace_size(b, h, L, d, B, kappa)), dtype=torch.uint8,
+                         device=dev)
+    o, lse = torch.empty_like(qd), torch.empty((b, h, L), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def sel():
+        bsb.ba_select_into(qd, kd, B, kappa, 1.0, 3, 0, perm_q, perm_k, idx, mask, None, ws_sel)
+
+    def att():
+        bsb.ba_sparse_attn_into(qd, kd, vd, B, perm_q, perm_k, idx, 0.0, o, lse, ws_att)
+    for _ in range(3):
+        sel()
+        att()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        sel()
+        e[1].record(stream)
+        att()
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    st, word = bsb.last_device_error(dev)
+    if st != 0:
+        raise RuntimeError(f"device error word {word:#x} ({w.name})")
+    sel_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    att_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = statistics.median(e[0].elapsed_time(e[2]) for e in ev)
+    sizes = np.full(N, B, dtype=np.float64)
+    sizes[-1] = L - (N - 1) * B
+    pair_tokens = sizes[idx.cpu().numpy()].sum(axis=-1)
+    flops = float(4.0 * d * (pair_tokens * sizes[None, None, :]).sum())
+    od, lsed = torch.empty_like(qd), torch.empty_like(lse)
+    bsb.ba_attn_dense_into(qd, kd, vd, 0.0, od, lsed)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(dense_steps):
+        bsb.ba_attn_dense_into(qd, kd, vd, 0.0, od, lsed)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = e0.elapsed_time(e1) / dense_steps
+    pk = peaks()
+    att_tf = flops / (att_ms * 1e-3) / 1e12
+    sb = select_bytes(w, kappa=kappa)
+    out = dict(workload=f"{w.name}: b{b} h{h} L{L} d{d} B{B} kappa{kappa} ({int(round(sparsity * 100))}% sparsity)",
+               step_ms=round(step_ms, 4), select_ms=round(sel_ms, 4), attn_ms=round(att_ms, 4),
+               attn_actual_tflops=round(att_tf, 2), attn_frac_tensor_burst=round(att_tf / pk["bf16"], 4),
+               step_frac_tensor_burst=round(flops / (step_ms * 1e-3) / 1e12 / pk["bf16"], 4),
+               select_gbs=round(sb / (sel_ms * 1e-3) / 1e9, 1),
+               select_frac_hbm_measured=round(sb / (sel_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+               dense_ms=round(dense_ms, 4),
+               dense_frac_tensor_burst=round(4.0 * b * h * L * L * d / (dense_ms * 1e-3) / 1e12 / pk["bf16"], 4),
+               speedup_vs_dense=round(dense_ms / step_ms, 3), density=round(flops / (4.0 * b * h * L * L * d), 4))
+    if with_cpu:
+        # the two smallest workloads in full; the others as one head's
+        # selection in full plus sampled attention, extrapolated
+        c = (cpu_oracle_full(w, q, k, v, kappa) if w.index <= 2
+             else cpu_oracle_sample(w, q, k, v, budget_s=cpu_budget_s, kappa=kappa))
+        out["cpu_oracle"] = dict(ms_per_step=round(c["ms_per_step"], 1), extrapolated=c["extrapolated"],
+                                 cores=c["cores"], sample=c["sample"])
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -267,6 +398,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dense-steps", type=int, default=3)
     ap.add_argument("--no-fidelity", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload detail (all five shapes, each sparsity)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -542,6 +675,15 @@ def main():
                    bound_dev_corr_unsorted=round(corr(f_plain), 4),
                    dev_over_bound_sorted=round(float((f_sorted["dev_max"] / f_sorted["bound"]).double().mean()), 4))
         del f_sorted, f_plain, sel0, lse_dense
+    # ---- every workload of the table, each sparsity (its own step) ----------
+    per_workload = {}
+    if not args.no_workloads:
+        with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+        for wn in ("tiny", "llada", "long32k", "video"):
+            ww = workloads.get(wn)
+            for sp in ww.sparsities:
+                per_workload[f"{wn}@{int(round(sp * 100))}"] = measure_workload(bsb, ww, sp, dev, with_cpu=with_cpu)
+                torch.cuda.empty_cache()
     h2d = 3 * q.numel() * q.element_size()
     d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
 
@@ -587,10 +729,13 @@ def main():
             **variant_ms,
             active_tokens_ms=round(losa_ms, 4),
             active_tokens_gbs=round(losa_bytes / (losa_ms * 1e-3) / 1e9, 1),
-            active_tokens_frac_hbm_measured=round(losa_bytes / (losa_ms * 1e-3) / 1e9 / peaks()["hbm"], 4),
+            # against the measured copy bandwidth (read + write); a read-mostly
+            # kernel can exceed 1.0 of it
+            active_tokens_frac_of_copy_bw=round(losa_bytes / (losa_ms * 1e-3) / 1e9 / peaks()["hbm"], 4),
             isolated_select=f"prefill {pre} tokens, kappa {kpre} + {kgen}, sort QK",
             **fid,
-            density=round(attn_flops / flops_step, 4)),
+            density=round(attn_flops / flops_step, 4),
+            workloads=per_workload),
     )
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = {kk: vv for kk, vv in cpu_oracle_sample(w, q, k, v).items() if kk != "seconds"}

@@ -109,6 +109,20 @@ def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
+class _on_device:
+    """Makes a tensor's device current around a library call (the library
+    launches on the current device and the caller's stream of that device)."""
+
+    def __init__(self, t):
+        self.ctx = _torch().cuda.device(t.device)
+
+    def __enter__(self):
+        self.ctx.__enter__()
+
+    def __exit__(self, *exc):
+        return self.ctx.__exit__(*exc)
+
+
 def _check(status: int, where: str):
     if status != 0:
         raise BAError(status, where)
@@ -142,9 +156,10 @@ def ba_select_into(q, k, block, kappa, beta, sort_mode, sort_window, perm_q, per
     _need_cuda(q, k, perm_q, perm_k, block_idx, block_mask, block_scores, workspace)
     b, h, L, d = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.ba_select(_ptr(q), _ptr(k), b, h, L, d, block, kappa, float(beta), sort_mode, sort_window,
-                       _ptr(perm_q), _ptr(perm_k), _ptr(block_idx), _ptr(block_mask),
-                       _ptr(block_scores), _ptr(workspace), ws_bytes, _stream(q.device))
+    with _on_device(q):
+        st = lib.ba_select(_ptr(q), _ptr(k), b, h, L, d, block, kappa, float(beta), sort_mode, sort_window,
+                           _ptr(perm_q), _ptr(perm_k), _ptr(block_idx), _ptr(block_mask),
+                           _ptr(block_scores), _ptr(workspace), ws_bytes, _stream(q.device))
     _check(st, "ba_select")
 
 
@@ -155,10 +170,11 @@ def ba_select_isolated_into(q, k, block, prefill_len, kappa_prefill, kappa_gener
     _need_cuda(q, k, perm_q, perm_k, block_idx, block_mask, block_scores, workspace)
     b, h, L, d = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.ba_select_isolated(_ptr(q), _ptr(k), b, h, L, d, block, prefill_len, kappa_prefill,
-                                kappa_generation, float(beta), sort_mode, sort_window, _ptr(perm_q),
-                                _ptr(perm_k), _ptr(block_idx), _ptr(block_mask), _ptr(block_scores),
-                                _ptr(workspace), ws_bytes, _stream(q.device))
+    with _on_device(q):
+        st = lib.ba_select_isolated(_ptr(q), _ptr(k), b, h, L, d, block, prefill_len, kappa_prefill,
+                                    kappa_generation, float(beta), sort_mode, sort_window, _ptr(perm_q),
+                                    _ptr(perm_k), _ptr(block_idx), _ptr(block_mask), _ptr(block_scores),
+                                    _ptr(workspace), ws_bytes, _stream(q.device))
     _check(st, "ba_select_isolated")
 
 
@@ -212,9 +228,10 @@ def ba_block_fidelity(q, k, block, lse, perm_q=None, perm_k=None, block_idx=None
     kappa = 0 if block_idx is None else block_idx.shape[-1]
     ws = _workspace(int(lib.ba_block_fidelity_workspace_size(b, h, L, d, block)), dev)
     ws_bytes = ws.numel() * ws.element_size()
-    st = lib.ba_block_fidelity(_ptr(q), _ptr(k), b, h, L, d, block, _ptr(perm_q), _ptr(perm_k), _ptr(lse),
-                               float(scale), _ptr(block_idx), kappa, _ptr(out["mass"]), _ptr(out["dev_max"]),
-                               _ptr(out["bound"]), _ptr(out["recall"]), _ptr(ws), ws_bytes, _stream(dev))
+    with _on_device(q):
+        st = lib.ba_block_fidelity(_ptr(q), _ptr(k), b, h, L, d, block, _ptr(perm_q), _ptr(perm_k), _ptr(lse),
+                                   float(scale), _ptr(block_idx), kappa, _ptr(out["mass"]), _ptr(out["dev_max"]),
+                                   _ptr(out["bound"]), _ptr(out["recall"]), _ptr(ws), ws_bytes, _stream(dev))
     _check(st, "ba_block_fidelity")
     return {kk: vv for kk, vv in out.items() if vv is not None}
 
@@ -229,8 +246,9 @@ def ba_active_tokens(q_now, q_prev, group, top_k, return_mse=False):
     b, h, L, d = q_now.shape
     active = torch.empty((b, h, L), dtype=torch.uint8, device=q_now.device)
     mse = torch.empty((b, h, L), dtype=torch.float32, device=q_now.device) if return_mse else None
-    st = lib.ba_active_tokens(_ptr(q_now), _ptr(q_prev), b, h, L, d, group, top_k, _ptr(active),
-                              _ptr(mse), _stream(q_now.device))
+    with _on_device(q_now):
+        st = lib.ba_active_tokens(_ptr(q_now), _ptr(q_prev), b, h, L, d, group, top_k, _ptr(active),
+                                  _ptr(mse), _stream(q_now.device))
     _check(st, "ba_active_tokens")
     return (active, mse) if return_mse else active
 
@@ -242,8 +260,9 @@ def ba_reuse_rows(o_new, lse_new, active, o_cache, lse_cache):
     _need_cuda(o_new, lse_new, active, o_cache, lse_cache)
     d = o_new.shape[-1]
     rows = o_new.numel() // d
-    st = lib.ba_reuse_rows(_ptr(o_new), _ptr(lse_new), _ptr(active), rows, d, _ptr(o_cache),
-                           _ptr(lse_cache), _stream(o_new.device))
+    with _on_device(o_new):
+        st = lib.ba_reuse_rows(_ptr(o_new), _ptr(lse_new), _ptr(active), rows, d, _ptr(o_cache),
+                               _ptr(lse_cache), _stream(o_new.device))
     _check(st, "ba_reuse_rows")
 
 
@@ -254,9 +273,10 @@ def ba_select_noalloc_into(q, k, block, kappa, beta, sort_mode, sort_window, per
     lib = load()
     _need_cuda(q, k, perm_q, perm_k, block_idx, block_mask, block_scores)
     b, h, L, d = q.shape
-    st = lib.ba_select_noalloc(_ptr(q), _ptr(k), b, h, L, d, block, kappa, float(beta), sort_mode,
-                               sort_window, _ptr(perm_q), _ptr(perm_k), _ptr(block_idx),
-                               _ptr(block_mask), _ptr(block_scores), _stream(q.device))
+    with _on_device(q):
+        st = lib.ba_select_noalloc(_ptr(q), _ptr(k), b, h, L, d, block, kappa, float(beta), sort_mode,
+                                   sort_window, _ptr(perm_q), _ptr(perm_k), _ptr(block_idx),
+                                   _ptr(block_mask), _ptr(block_scores), _stream(q.device))
     _check(st, "ba_select_noalloc")
 
 
@@ -295,9 +315,10 @@ def ba_sparse_attn_into(q, k, v, block, perm_q, perm_k, block_idx, scale, o, lse
     b, h, L, d = q.shape
     kappa = block_idx.shape[-1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = lib.ba_sparse_attn(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, block, _ptr(perm_q), _ptr(perm_k),
-                            _ptr(block_idx), kappa, float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
-                            ws_bytes, _stream(q.device))
+    with _on_device(q):
+        st = lib.ba_sparse_attn(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, block, _ptr(perm_q), _ptr(perm_k),
+                                _ptr(block_idx), kappa, float(scale), _ptr(o), _ptr(lse), _ptr(workspace),
+                                ws_bytes, _stream(q.device))
     _check(st, "ba_sparse_attn")
 
 
@@ -319,8 +340,9 @@ def ba_attn_dense_into(q, k, v, scale, o, lse):
     lib = load()
     _need_cuda(q, k, v, o, lse)
     b, h, L, d = q.shape
-    st = lib.ba_attn_dense(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, float(scale), _ptr(o), _ptr(lse),
-                           _stream(q.device))
+    with _on_device(q):
+        st = lib.ba_attn_dense(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, float(scale), _ptr(o), _ptr(lse),
+                               _stream(q.device))
     _check(st, "ba_attn_dense")
 
 
@@ -341,8 +363,9 @@ def ba_merge_lse_into(o1, lse1, o2, lse2, o, lse):
     _need_cuda(o1, lse1, o2, lse2, o, lse)
     d = o1.shape[-1]
     rows = o1.numel() // d
-    st = lib.ba_merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), rows, d, _ptr(o), _ptr(lse),
-                          _stream(o1.device))
+    with _on_device(o1):
+        st = lib.ba_merge_lse(_ptr(o1), _ptr(lse1), _ptr(o2), _ptr(lse2), rows, d, _ptr(o), _ptr(lse),
+                              _stream(o1.device))
     _check(st, "ba_merge_lse")
 
 
@@ -372,8 +395,10 @@ def selftest_attn_stall(q, k, v, o, lse, limit_us=1000):
     lib = load()
     _need_cuda(q, k, v, o, lse)
     b, h, L, d = q.shape
-    _check(lib.ba_selftest_attn_stall(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, int(limit_us), _ptr(o),
-                                      _ptr(lse), _stream(q.device)), "ba_selftest_attn_stall")
+    with _on_device(q):
+        st = lib.ba_selftest_attn_stall(_ptr(q), _ptr(k), _ptr(v), b, h, L, d, int(limit_us), _ptr(o),
+                                        _ptr(lse), _stream(q.device))
+    _check(st, "ba_selftest_attn_stall")
 
 
 def last_device_error(device=None):

@@ -15,19 +15,31 @@
 
 namespace ba {
 
+// In place (o may be o1 or o2, lse may be lse1 or lse2): each lane reads and
+// writes only its own 16 bytes of O, but lane 0 of a row writes the row's LSE
+// that the row's other lanes read, so every lane reads its inputs before the
+// warp barrier and writes after it (the VPR lanes of a row lie in one warp).
+// No __restrict__ or read-only loads on pointers that may alias.
 template <int D>
-__global__ void __launch_bounds__(256) k_merge_lse(const __nv_bfloat16 *__restrict__ o1,
-                                                   const float *__restrict__ lse1,
-                                                   const __nv_bfloat16 *__restrict__ o2,
-                                                   const float *__restrict__ lse2, int64_t rows,
-                                                   __nv_bfloat16 *__restrict__ o,
-                                                   float *__restrict__ lse) {
+__global__ void __launch_bounds__(256) k_merge_lse(const __nv_bfloat16 *o1, const float *lse1,
+                                                   const __nv_bfloat16 *o2, const float *lse2,
+                                                   int64_t rows, __nv_bfloat16 *o, float *lse) {
   constexpr int VPR = D / 8;
+  static_assert(32 % VPR == 0, "a row's lanes lie in one warp");
   const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t row = gid / VPR;
   const int c = static_cast<int>(gid % VPR);
-  if (row >= rows) return;
-  const float a = __ldg(lse1 + row), b = __ldg(lse2 + row);
+  const bool valid = row < rows;
+  float a = -INFINITY, b = -INFINITY;
+  uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+  if (valid) {
+    a = lse1[row];
+    b = lse2[row];
+    x = reinterpret_cast<const uint4 *>(o1 + row * D)[c];
+    y = reinterpret_cast<const uint4 *>(o2 + row * D)[c];
+  }
+  __syncwarp();
+  if (!valid) return;
   const float m = fmaxf(a, b);
   float w1 = 0.f, w2 = 0.f, l = -INFINITY;
   if (m != -INFINITY) {
@@ -37,8 +49,6 @@ __global__ void __launch_bounds__(256) k_merge_lse(const __nv_bfloat16 *__restri
     w2 = e2 / s;
     l = m + logf(s);
   }
-  const uint4 x = __ldg(reinterpret_cast<const uint4 *>(o1 + row * D) + c);
-  const uint4 y = __ldg(reinterpret_cast<const uint4 *>(o2 + row * D) + c);
   const __nv_bfloat162 *hx = reinterpret_cast<const __nv_bfloat162 *>(&x);
   const __nv_bfloat162 *hy = reinterpret_cast<const __nv_bfloat162 *>(&y);
   uint4 r;

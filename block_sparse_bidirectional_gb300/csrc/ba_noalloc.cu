@@ -54,6 +54,15 @@ extern "C" int ba_select_noalloc(const void *q, const void *k, int batch, int he
   const size_t need = ba_select_workspace_size(batch, heads, seqlen, head_dim, block, kappa,
                                                sort_mode, sort_window);
   if (need > static_cast<size_t>(BA_SELECT_STATIC_SCRATCH_BYTES)) return BA_ERR_WORKSPACE;
+  // the scratch address is per device: the stream must belong to the
+  // current device (else the kernels would be given another GPU's array)
+  if (stream != nullptr) {
+    int cur = 0, sdev = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess ||
+        cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+      return BA_ERR_CUDA;
+    if (sdev != cur) return BA_ERR_INVALID_ARG;
+  }
   void *scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
   if (st != BA_OK) return st;

@@ -126,7 +126,8 @@ int ba_select(const void *q, const void *k, int batch, int heads, int seqlen,
  *  - The first call on a device looks up that device's copy of the array
  *    (cudaGetSymbolAddress with the device current) and caches it; make that
  *    first call before any stream capture begins.  The current device must be
- *    the device of `stream`.
+ *    the device of `stream`; a stream of another device returns
+ *    BA_ERR_INVALID_ARG and launches nothing.
  *  - The library allocates and frees nothing in this call.
  *  - Every call on a device shares the one array: calls whose work overlaps on
  *    the GPU (different streams, or different host threads) race on it and

@@ -254,6 +254,28 @@ def test_merge_lse_kernel_against_oracle(dev):
         assert np.all(og[both.numpy()] == 0) and np.all(np.isneginf(lg[both.numpy()]))
 
 
+def test_merge_lse_in_place_equals_out_of_place(dev):
+    """ba_merge_lse writing over its first (or second) input gives the same
+    bits as writing to fresh outputs (the in-place use include/ba.h allows)."""
+    gen = torch.Generator().manual_seed(22)
+    for d in (64, 128):
+        rows = 4099
+        o1 = torch.randn((rows, d), generator=gen).to(torch.bfloat16).to(dev)
+        o2 = torch.randn((rows, d), generator=gen).to(torch.bfloat16).to(dev)
+        l1 = (torch.randn(rows, generator=gen) * 4).to(dev)
+        l2 = (torch.randn(rows, generator=gen) * 4).to(dev)
+        l1[::7] = -float("inf")
+        ref_o, ref_l = bsb.ba_merge_lse(o1, l1, o2, l2)
+        a_o, a_l = o1.clone(), l1.clone()
+        bsb.ba_merge_lse_into(a_o, a_l, o2, l2, a_o, a_l)      # over the first input
+        b_o, b_l = o2.clone(), l2.clone()
+        bsb.ba_merge_lse_into(o1, l1, b_o, b_l, b_o, b_l)      # over the second input
+        torch.cuda.synchronize()
+        for og, lg in ((a_o, a_l), (b_o, b_l)):
+            assert torch.equal(og, ref_o)
+            assert torch.equal(torch.nan_to_num(lg, neginf=-1e30), torch.nan_to_num(ref_l, neginf=-1e30))
+
+
 def test_merge_lse_kernel_joins_split_lists(dev):
     """Attention over the two halves of every list, merged on the GPU, equals
     the single call over the whole list (within the attention tolerances)."""
