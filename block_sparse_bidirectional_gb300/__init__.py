@@ -23,7 +23,7 @@ __all__ = ["load", "ba_select", "ba_select_into", "ba_select_noalloc_into", "ba_
            "ba_select_isolated_into", "ba_sparse_attn", "ba_sparse_attn_into", "ba_block_fidelity",
            "ba_active_tokens", "ba_reuse_rows",
            "ba_attn_dense", "ba_attn_dense_into", "ba_merge_lse", "ba_merge_lse_into",
-           "last_device_error", "selftest_wait_timeout", "selftest_attn_stall", "BAError",
+           "last_device_error", "selftest_wait_timeout", "ba_validate_selection", "selftest_attn_stall", "BAError",
            "SORT_NONE", "SORT_K", "SORT_Q", "SORT_QK", "select_workspace_size",
            "sparse_attn_workspace_size", "header_functions", "LIB_PATH"]
 
@@ -46,6 +46,7 @@ _SIGS = {
     "ba_attn_dense": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [_c_float] + [_c_void_p] * 3),
     "ba_last_device_error": (_c_int, [_c_void_p, _c_u32p]),
     "ba_selftest_wait_timeout": (_c_int, [ctypes.c_uint32, _c_void_p]),
+    "ba_validate_selection": (_c_int, [_c_void_p] * 3 + [_c_int] * 5 + [_c_u32p, _c_void_p]),
     "ba_selftest_attn_stall": (_c_int, [_c_void_p] * 3 + [_c_int] * 4 + [ctypes.c_uint32] + [_c_void_p] * 3),
     "ba_merge_lse": (_c_int, [_c_void_p] * 4 + [ctypes.c_int64, _c_int] + [_c_void_p] * 3),
     "ba_select_isolated": (_c_int, [_c_void_p, _c_void_p] + [_c_int] * 8 + [_c_float, _c_int, _c_int]
@@ -376,6 +377,24 @@ def ba_merge_lse(o1, lse1, o2, lse2):
     lse = torch.empty_like(lse1)
     ba_merge_lse_into(o1, lse1, o2, lse2, o, lse)
     return o, lse
+
+
+def ba_validate_selection(block, block_idx, perm_q=None, perm_k=None):
+    """Checks a selection on the device (pi_q, pi_k permutations; each row of
+    block_idx strictly ascending with ids < N).  Returns (status, detail):
+    status 0 when every check passes, else BA_ERR_INVALID_ARG (1) with detail
+    bits 1 pi_q, 2 pi_k, 4 block_idx.  Synchronous."""
+    lib = load()
+    _need_cuda(block_idx, perm_q, perm_k)
+    b, h, N, kappa = block_idx.shape
+    L = perm_q.shape[-1] if perm_q is not None else (perm_k.shape[-1] if perm_k is not None else N * block)
+    word = ctypes.c_uint32(0)
+    with _on_device(block_idx):
+        st = lib.ba_validate_selection(_ptr(perm_q), _ptr(perm_k), _ptr(block_idx), b, h, L, block, kappa,
+                                       ctypes.byref(word), _stream(block_idx.device))
+    if st not in (0, 1):
+        raise BAError(st, "ba_validate_selection")
+    return st, word.value
 
 
 def selftest_wait_timeout(limit_us=1000, device=None):

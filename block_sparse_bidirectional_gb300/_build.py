@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(OUT_DIR, "libba.so")
 BUILD_DIR = os.path.join(OUT_DIR, "obj")
 
 SOURCES = ["ba_api.cu", "ba_select.cu", "ba_attn.cu", "ba_noalloc.cu", "ba_merge.cu", "ba_fidelity.cu", "ba_losa.cu",
-           "ba_selftest.cu"]
+           "ba_selftest.cu", "ba_validate.cu"]
 HEADERS = ["ba_common.cuh", "ba_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",

@@ -348,6 +348,24 @@ int ba_merge_lse(const void *o1, const float *lse1, const void *o2, const float 
                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int ba_validate_selection(const int32_t *perm_q, const int32_t *perm_k, const int32_t *block_idx,
+                          int batch, int heads, int seqlen, int block, int kappa, uint32_t *detail,
+                          ba_stream_t stream) {
+  if (detail) *detail = 0;
+  int st = check_shape(batch, heads, seqlen, 64, block);
+  if (st != BA_OK) return st;
+  const int n = (seqlen + block - 1) / block;
+  if (kappa < 1 || kappa > n) return BA_ERR_INVALID_ARG;
+  if (!block_idx || !aligned16(block_idx) || (perm_q && !aligned16(perm_q)) || (perm_k && !aligned16(perm_k)))
+    return BA_ERR_INVALID_ARG;
+  uint32_t word = 0;
+  if (run_validate_selection(perm_q, perm_k, block_idx, static_cast<int64_t>(batch) * heads, seqlen, n, kappa,
+                             &word, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return BA_ERR_CUDA;
+  if (detail) *detail = word;
+  return word ? BA_ERR_INVALID_ARG : BA_OK;
+}
+
 int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream) {
   if (limit_us < 1 || limit_us > 1000000) return BA_ERR_INVALID_ARG;
   return map_cuda(run_selftest_wait(static_cast<uint64_t>(limit_us) * 1000ull,

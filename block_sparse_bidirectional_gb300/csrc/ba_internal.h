@@ -88,6 +88,11 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st);
 // attention kernel's bounded-wait unwind (see ba_selftest_attn_stall).
 cudaError_t run_attention_stall(const AttnArgs &a, uint64_t limit_ns, cudaStream_t st);
 
+// Checks pi_q, pi_k (nullable) and block_idx on the device, synchronises the
+// stream and returns the failure bits (1 pi_q, 2 pi_k, 4 block_idx) in *word.
+cudaError_t run_validate_selection(const int32_t *perm_q, const int32_t *perm_k, const int32_t *block_idx,
+                                   int64_t bh, int L, int N, int kappa, uint32_t *word, cudaStream_t st);
+
 cudaError_t run_merge_lse(const void *o1, const float *lse1, const void *o2, const float *lse2,
                           int64_t rows, int head_dim, void *o, float *lse, cudaStream_t st);
 

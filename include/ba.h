@@ -307,6 +307,29 @@ int ba_merge_lse(const void *o1, const float *lse1, const void *o2,
                  float *lse, ba_stream_t stream);
 
 /*
+ * Checks a selection's outputs before they are used: BA-Att paper Algorithm 1
+ * steps 1-2 make pi_q and pi_k permutations of each (b,h) sequence, and
+ * steps 8-11 keep kappa distinct key blocks per query block (ba_select emits
+ * them ascending).  ba_sparse_attn trusts these inputs: it never faults on
+ * them (out-of-range entries are clamped or dropped), but then its result is
+ * meaningless.  This call runs the checks on the device:
+ *   perm_q, perm_k  int32 [b,h,L] or NULL (not checked): every entry in
+ *                   [0, L) and no position twice in a sequence;
+ *   block_idx       int32 [b,h,N,kappa] (required): every row strictly
+ *                   ascending with ids in [0, N).
+ * It is synchronous: it enqueues the checks on `stream`, waits for the
+ * stream and returns BA_OK, or BA_ERR_INVALID_ARG with *detail (may be NULL)
+ * set to the failed checks: bit 0 pi_q, bit 1 pi_k, bit 2 block_idx.  Not
+ * for use during stream capture; concurrent calls share one device word and
+ * must be serialised.  block is 64 or 128; shape limits as elsewhere
+ * (BA_ERR_UNSUPPORTED / BA_ERR_INVALID_ARG before any launch).
+ */
+int ba_validate_selection(const int32_t *perm_q, const int32_t *perm_k,
+                          const int32_t *block_idx, int batch, int heads,
+                          int seqlen, int block, int kappa, uint32_t *detail,
+                          ba_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word that
  * kernels set when a bounded wait gives up.  Returns BA_OK,
  * BA_ERR_DEVICE_TIMEOUT or BA_ERR_CUDA.  `detail` (may be NULL) receives the

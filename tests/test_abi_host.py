@@ -257,3 +257,16 @@ def test_selftest_rejects_limits_outside_range():
     lib = bsb.load()
     for bad in (0, 1000001, 2**32 - 1):
         assert lib.ba_selftest_wait_timeout(bad, None) == INVALID
+
+
+def test_validate_selection_rejects_before_launch():
+    lib = bsb.load()
+    u = ctypes.c_uint32(7)
+    # block_idx is required; kappa within [1, N]; block 64 or 128; aligned pointers
+    assert lib.ba_validate_selection(P, P, None, 1, 1, 1024, 64, 8, ctypes.byref(u), None) == INVALID
+    assert u.value == 0
+    assert lib.ba_validate_selection(P, P, P, 1, 1, 1024, 64, 0, None, None) == INVALID
+    assert lib.ba_validate_selection(P, P, P, 1, 1, 1024, 64, 17, None, None) == INVALID
+    assert lib.ba_validate_selection(P, P, P, 1, 1, 1024, 32, 8, None, None) == UNSUPPORTED
+    assert lib.ba_validate_selection(MIS, P, P, 1, 1, 1024, 64, 8, None, None) == INVALID
+    assert lib.ba_validate_selection(P, P, MIS, 1, 1, 1024, 64, 8, None, None) == INVALID
