@@ -29,6 +29,7 @@
 //                   select of the kappa-th largest score on order-preserving
 //                   integer keys (warp reductions), ties to the lower block
 //                   index; emits the ascending index list and the bitmask.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -308,6 +309,227 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__
       perm[pbase + o_cta + i] = static_cast<int32_t>(s_out[spad(i)] & 0xffffffffu);
     else
       out[base + o_cta + i] = s_out[spad(i)];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// step 1-2, long windows: stable LSD radix sort on the 32 norm bits of the
+// 64-bit keys (norm bits << 32 | token index), four passes of 8-bit digits.
+// A cluster of kRadixCluster CTAs sorts one window: CTA r owns the r-th
+// contiguous part of it and each of its warps a contiguous slice of that, so
+// the order "CTA, warp, position" is the input order.  Per pass: every warp
+// counts its digits (lanes with equal digits found with eight ballots, so
+// one lane per digit adds); the CTAs exchange their digit totals through
+// distributed shared memory; each (warp, digit) gets its first output
+// position; a second sweep writes every key at that position plus its rank
+// among the equal digits of its 32-key chunk.  Equal norms keep the input
+// (token index) order, the order the keys start in.  The last pass writes pi.
+// grid = (kRadixCluster * windows, sorted sequences)
+// ---------------------------------------------------------------------------
+constexpr int kRadixThreads = 1024;
+constexpr int kRadixWarps = kRadixThreads / 32;
+constexpr int kRadixCluster = 4;
+constexpr int kRadixBins = 256;
+// Parts of up to kRadixStage keys (windows up to 4 x 16384 tokens) keep each
+// warp's keys in registers across both sweeps (kRadixRegChunks chunks of 32
+// per warp) and leave through a shared-memory stage in digit order, so each
+// digit's keys go out as one contiguous, coalesced run; longer parts reload
+// their keys and scatter them directly.
+constexpr int kRadixRegChunks = 16;
+constexpr int kRadixStage = kRadixWarps * kRadixRegChunks * 32;
+constexpr size_t kRadixSmem =
+    sizeof(int) * (kRadixWarps * kRadixBins + 3 * kRadixBins + kRadixBins / 32) + sizeof(uint64_t) * kRadixStage;
+
+__global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixThreads)
+    k_radix_pass(const uint64_t *__restrict__ in, uint64_t *__restrict__ out, int32_t *__restrict__ perm0,
+                 int32_t *__restrict__ perm1, SortGeom g, int shift, int final_pass) {
+  namespace cg = cooperative_groups;
+  extern __shared__ __align__(16) uint8_t rsm[];
+  uint64_t *stage = reinterpret_cast<uint64_t *>(rsm);                  // [kRadixStage]
+  int(*hist)[kRadixBins] = reinterpret_cast<int(*)[kRadixBins]>(stage + kRadixStage);  // [warps][bins]
+  int *total = &hist[kRadixWarps][0];   // this CTA's digit counts (read by the cluster)
+  int *lbase = total + kRadixBins;      // first staged position of each digit
+  int *delta = lbase + kRadixBins;      // output position - staged position, per digit
+  int *wsum = delta + kRadixBins;       // [kRadixBins / 32]
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = static_cast<int>(cluster.block_rank());
+  const int w = blockIdx.x / kRadixCluster;
+  const int seq = blockIdx.y;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int wlen = window_len(g, w);
+  const int64_t base = static_cast<int64_t>(seq) * g.L + window_start(g, w);
+  // this CTA's part and this warp's slice of it
+  const int p0 = static_cast<int>(static_cast<int64_t>(wlen) * r / kRadixCluster);
+  const int p1 = static_cast<int>(static_cast<int64_t>(wlen) * (r + 1) / kRadixCluster);
+  const int s0 = p0 + static_cast<int>(static_cast<int64_t>(p1 - p0) * warp / kRadixWarps);
+  const int s1 = p0 + static_cast<int>(static_cast<int64_t>(p1 - p0) * (warp + 1) / kRadixWarps);
+  // uniform over the cluster (all its parts differ in length by at most one)
+  const bool staged = (wlen + kRadixCluster - 1) / kRadixCluster <= kRadixStage;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  auto digit = [&](uint64_t key) { return static_cast<int>((key >> (32 + shift)) & 0xFFu); };
+  // lanes of `m` whose digit equals this lane's: eight ballots, one per
+  // digit bit (a constant cost, whatever the number of distinct digits;
+  // measured faster than match.any on the low, near-uniform digits)
+  auto same_digit = [&](uint32_t m, int dig) {
+    // a chunk of one digit (the common case for the exponent byte)
+    if (__all_sync(m, dig == __shfl_sync(m, dig, __ffs(m) - 1))) return m;
+    uint32_t peers = m;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const uint32_t v = __ballot_sync(m, (dig >> b) & 1);
+      peers &= ((dig >> b) & 1) ? v : ~v;
+    }
+    return peers;
+  };
+  for (int i = lane; i < kRadixBins; i += 32) hist[warp][i] = 0;
+  __syncwarp();
+  // ---- sweep 1: per-warp digit counts (staged: keys kept in registers) ----
+  uint64_t kr[kRadixRegChunks];
+  if (staged) {
+#pragma unroll
+    for (int u = 0; u < kRadixRegChunks; ++u) {
+      const int i = s0 + u * 32 + lane;
+      kr[u] = (i < s1) ? in[base + i] : 0ull;
+    }
+#pragma unroll
+    for (int u = 0; u < kRadixRegChunks; ++u) {
+      const int i = s0 + u * 32 + lane;
+      if (s0 + u * 32 >= s1) break;  // uniform over the warp
+      const bool act = i < s1;
+      const uint32_t m = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const int dig = digit(kr[u]);
+        const uint32_t peers = same_digit(m, dig);
+        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
+      }
+      __syncwarp();  // the next chunk's leader of a digit sees this update
+    }
+  } else {
+    for (int c = s0; c < s1; c += 32) {
+      const int i = c + lane;
+      const bool act = i < s1;
+      const uint32_t m = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const int dig = digit(in[base + i]);
+        const uint32_t peers = same_digit(m, dig);
+        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // ---- this CTA's totals; per-warp counts become exclusive prefixes ----
+  if (threadIdx.x < kRadixBins) {
+    const int d = threadIdx.x;
+    int run = 0;
+    for (int k = 0; k < kRadixWarps; ++k) {
+      const int v = hist[k][d];
+      hist[k][d] = run;
+      run += v;
+    }
+    total[d] = run;
+  }
+  cluster.sync();  // every CTA's totals are visible to the cluster
+  int before = 0, all = 0, mine = 0;
+  if (threadIdx.x < kRadixBins) {
+    const int d = threadIdx.x;
+    for (int k = 0; k < kRadixCluster; ++k) {
+      const int v = cluster.map_shared_rank(total, k)[d];
+      all += v;
+      if (k < r) before += v;
+      if (k == r) mine = v;
+    }
+  }
+  cluster.sync();  // the remote reads are done before any CTA moves on (or exits)
+  // exclusive scans over the 256 digits: of the window's totals (global
+  // positions) and of this CTA's totals (staged positions)
+  if (threadIdx.x < kRadixBins) {
+    int incl = all, incl_m = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      const int vm = __shfl_up_sync(0xffffffffu, incl_m, off);
+      if (lane >= off) {
+        incl += v;
+        incl_m += vm;
+      }
+    }
+    if (lane == 31) wsum[warp] = incl;
+    total[threadIdx.x] = incl - all + before;
+    lbase[threadIdx.x] = incl_m - mine;
+    if (lane == 31) delta[warp] = incl_m;  // borrowed: the warp's sum of this CTA's totals
+  }
+  __syncthreads();
+  int first = 0, lfirst = 0;
+  if (threadIdx.x < kRadixBins) {
+    int off = 0, off_m = 0;
+    for (int k = 0; k < warp; ++k) {
+      off += wsum[k];
+      off_m += delta[k];
+    }
+    first = total[threadIdx.x] + off;      // this CTA's first output position for the digit
+    lfirst = lbase[threadIdx.x] + off_m;   // its first staged position for the digit
+  }
+  __syncthreads();  // every thread has read delta[] (the warp sums) before it is overwritten
+  if (threadIdx.x < kRadixBins) {
+    const int d = threadIdx.x;
+    if (staged) {
+      delta[d] = first - lfirst;
+      for (int k = 0; k < kRadixWarps; ++k) hist[k][d] += lfirst;
+    } else {
+      for (int k = 0; k < kRadixWarps; ++k) hist[k][d] += first;
+    }
+  }
+  __syncthreads();
+  // ---- sweep 2: rank in input order; stage and write out in digit runs ----
+  int32_t *perm = (seq < g.bh) ? perm0 : perm1;
+  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w);
+  if (staged) {
+#pragma unroll
+    for (int u = 0; u < kRadixRegChunks; ++u) {
+      const int i = s0 + u * 32 + lane;
+      if (s0 + u * 32 >= s1) break;
+      const bool act = i < s1;
+      const uint32_t m = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const int dig = digit(kr[u]);
+        const uint32_t peers = same_digit(m, dig);
+        const int dest = hist[warp][dig] + __popc(peers & lt_mask);
+        __syncwarp(m);
+        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
+        stage[dest] = kr[u];
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    const int n = p1 - p0;
+    for (int t = threadIdx.x; t < n; t += kRadixThreads) {
+      const uint64_t key = stage[t];
+      const int dest = t + delta[digit(key)];
+      if (final_pass)
+        perm[pbase + dest] = static_cast<int32_t>(key & 0xffffffffu);
+      else
+        out[base + dest] = key;
+    }
+  } else {
+    for (int c = s0; c < s1; c += 32) {
+      const int i = c + lane;
+      const bool act = i < s1;
+      const uint32_t m = __ballot_sync(0xffffffffu, act);
+      if (act) {
+        const uint64_t key = in[base + i];
+        const int dig = digit(key);
+        const uint32_t peers = same_digit(m, dig);
+        const int dest = hist[warp][dig] + __popc(peers & lt_mask);
+        __syncwarp(m);
+        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
+        if (final_pass)
+          perm[pbase + dest] = static_cast<int32_t>(key & 0xffffffffu);
+        else
+          out[base + dest] = key;
+      }
+      __syncwarp();
+    }
   }
 }
 
@@ -695,12 +917,32 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
     g.win = (win <= 0 || win >= L) ? L : win;
     g.nwin = (L + g.win - 1) / g.win;
   }
+  cudaError_t e;
+  if (g.win > kChunk) {
+    // long windows: four radix passes, keys -> buf0 -> buf1 -> buf0 -> pi
+    static std::atomic<uint64_t> radix_configured{0};
+    e = once_per_device(radix_configured, [] {
+      return cudaFuncSetAttribute(k_radix_pass, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kRadixSmem));
+    });
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(kRadixCluster * g.nwin), static_cast<unsigned>(nseq));
+    const uint64_t *src = keys;
+    uint64_t *bufs[2] = {buf0, buf1};
+    for (int pass = 0; pass < 4; ++pass) {
+      k_radix_pass<<<grid, kRadixThreads, kRadixSmem, st>>>(src, bufs[pass & 1], perm0, perm1, g, 8 * pass,
+                                                            pass == 3);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      src = bufs[pass & 1];
+    }
+    return cudaSuccess;
+  }
   int npasses = 0;
   for (int w = kChunk; w < g.win; w <<= 1) ++npasses;
   const int chunks = (g.win + kChunk - 1) / kChunk;
   const size_t smem = 2 * spad_size(kChunk) * sizeof(uint64_t);
   static std::atomic<uint64_t> configured{0};
-  cudaError_t e = once_per_device(configured, [smem] {
+  e = once_per_device(configured, [smem] {
     return cudaFuncSetAttribute(k_chunk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem));
   });
