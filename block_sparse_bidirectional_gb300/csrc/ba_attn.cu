@@ -24,7 +24,15 @@
 //                alternating tiles so the tensor core works on one tile
 //                while the other tile's softmax runs.  S_t(j+1) is issued
 //                right after PV_t(j) and overwrites P_t in place (tcgen05 MMAs
-//                of one thread execute in order).
+//                of one thread execute in order).  Descriptors are
+//                precomputed 32-bit words plus one add per MMA.
+//   warp 2 (3)   row gathers of Q', K', V' for this head's unclaimed slices
+//                and one slice of a later head (warps 2-3 in the packed
+//                64-token-block kernel).
+//   warp 3       (unpacked kernels) stage confirmer: waits for the K/V copies
+//                of each tile's next PV and S and adds the last arrival of
+//                that tile's P-ready barrier, so the MMA thread waits on one
+//                barrier per tile and iteration.
 //   warps 4-7,   softmax + epilogue for tile 0 and tile 1: thread r owns row r
 //   warps 8-11   (TMEM lane r).  Online softmax in the log2 domain with a lazy
 //                rescale: O_t is corrected only when the running max grows by
@@ -108,7 +116,8 @@ struct AttnParams {
   const uint16_t *pair_lists;  // [b*h][npairs][2][N]: per tile, common blocks first
   const int32_t *pair_counts;  // [b*h][npairs][4]: n0, n1, common, -
   const int32_t *perm_q;  // sorted query position -> original row (nullable)
-  // Row gathers inside the kernel by warps 2-3 (claim != nullptr): head h's
+  // Row gathers inside the kernel by warp 2 (unpacked) or warps 2-3
+  // (packed) (claim != nullptr): head h's
   // rows are cut into nslices slices of slice_rows rows.  A slice is claimed
   // with an atomic ticket on claim[h] and counted in done[h] once written.
   // CTAs of head h - lookahead each claim one slice ahead of time, and CTAs
@@ -137,14 +146,13 @@ struct AttnParams {
 // (k_pair_lists); dense tiles walk every block.
 __device__ __forceinline__ uint32_t dense_entry(int j) { return static_cast<uint32_t>(j) | (3u << 12); }
 
-// One CTA's share of the row gathers of head hp (64 threads, 16 bytes each
-// per access; kGatherUnroll rows per thread in flight).
-constexpr int kGatherUnroll = 4;
-
-template <int D>
+// One CTA's share of the row gathers of head hp (kGatherThreads threads,
+// 16 bytes each per access; 16 rows of the slice in flight per pass).
+template <int D, int kGatherThreads>
 __device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pair, int tid) {
-  constexpr int VPR = D / 8;      // 16-byte pieces per row
-  constexpr int RPP = 64 / VPR;   // rows per pass of the 64 threads
+  constexpr int kGatherUnroll = kGatherThreads == 32 ? 8 : 4;
+  constexpr int VPR = D / 8;                 // 16-byte pieces per row
+  constexpr int RPP = kGatherThreads / VPR;  // rows per pass of the gather threads
   const int c = tid % VPR, rsub = tid / VPR;
   const int64_t base = static_cast<int64_t>(hp) * p.L;
   const int r_begin = pair * p.slice_rows;
@@ -173,26 +181,42 @@ __device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pa
   }
 }
 
-// Named barrier of the two gather warps (id 0 is __syncthreads).
-__device__ __forceinline__ void gather_bar() { asm volatile("bar.sync 1, 64;" ::: "memory"); }
+// Gathers run on kGatherThreads threads (one warp, or warps 2-3): a named
+// barrier (id 1) of those threads, a ticket broadcast through shared memory.
+template <int kGatherThreads>
+__device__ __forceinline__ void gather_sync() {
+  if (kGatherThreads == 32)
+    __syncwarp();
+  else
+    asm volatile("bar.sync 1, %0;" ::"n"(kGatherThreads) : "memory");
+}
 
-// One ticket from `counter`, broadcast to the 64 gather threads.
+// One ticket from `counter`, broadcast to the gather threads.
+template <int kGatherThreads>
 __device__ __forceinline__ int claim_slice(int *counter, volatile int *bcast, int tid) {
-  if (tid == 0) *bcast = atomicAdd(counter, 1);
-  gather_bar();
-  const int s = *bcast;
-  gather_bar();  // every thread has read it before the next ticket overwrites it
-  return s;
+  if constexpr (kGatherThreads == 32) {
+    int s = 0;
+    if (tid == 0) s = atomicAdd(counter, 1);
+    return __shfl_sync(0xffffffffu, s, 0);
+  } else {
+    if (tid == 0) *bcast = atomicAdd(counter, 1);
+    gather_sync<kGatherThreads>();
+    const int s = *bcast;
+    gather_sync<kGatherThreads>();  // every thread has read it before the next ticket overwrites it
+    return s;
+  }
 }
 
 // Publish a written slice: after the barrier, one thread orders every gather
 // thread's stores before its count (fence cumulativity) and counts the slice.
+template <int kGatherThreads>
 __device__ __forceinline__ void publish_slice(int *done, int tid) {
-  gather_bar();
+  gather_sync<kGatherThreads>();
   if (tid == 0) {
     __threadfence();
     atomicAdd(done, 1);
   }
+  if (kGatherThreads == 32) __syncwarp();
 }
 
 template <int D, int BK, bool kDense, bool kPack>
@@ -201,6 +225,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
            const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
   using Lay = AttnLayout<D, BK>;
   constexpr int S = Lay::kSlots;
+  // Unpacked kernels (dense; 128-token blocks): warp 3 confirms every K/V
+  // copy and adds the last arrival of P-ready, so the MMA thread waits on
+  // P-ready alone, and warp 2 gathers rows.  Packed kernels (64-token
+  // blocks): the MMA thread waits for each copy itself and warps 2-3 gather
+  // (their CTAs are short, and one gather warp fell behind: 0.53 -> 1.13 ms
+  // on the LLaDA shape).
+  constexpr bool kConfirm = !kPack;
+  constexpr int kGatherThreads = kConfirm ? 32 : 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     for (int t = 0; t < kTiles; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], kTileM);
+      mbar_init(&p_full[t], kTileM + (kConfirm ? 1 : 0));  // the tile's softmax threads (and the confirmer)
       mbar_init(&o_done[t], 1);
     }
     mbar_init(drain, 1);
@@ -357,10 +389,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t lim = p.issuer_wait_ns;
       bool ok = mbar_wait(q_full, 0, kSiteQFull, abort_flag, lim);
       tc_fence_after();
-      auto take = [&](int &slot) -> bool {
+      // prologue takes wait for their K copies here; in the loop of an
+      // unpacked kernel a slot's copy is confirmed by the stage confirmer
+      // (warp 3) before its P-ready arrival, so the P wait covers it
+      auto take_wait = [&](int &slot) -> bool {
         slot = consumed % S;
         if (!mbar_wait(&slot_full[slot], (consumed / S) & 1, kSiteKFull, abort_flag, lim)) return false;
         tc_fence_after();
+        ++consumed;
+        return true;
+      };
+      auto take = [&](int &slot) -> bool {
+        if (!kConfirm) return take_wait(slot);
+        slot = consumed % S;
         ++consumed;
         return true;
       };
@@ -395,7 +436,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (n_t[t] == 0) continue;
         const bool sh = 0 < n_common;
         int sl = slot_k0;
-        if (!(sh && t == 1) && !(ok = take(sl))) break;
+        if (!(sh && t == 1) && !(ok = take_wait(sl))) break;
         mma_s(t, sl);
         if (!sh || t == 1) mma_commit(&slot_empty[sl]);
         else slot_k0 = sl;
@@ -424,26 +465,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       mma_commit(drain);
       mbar_wait_drain(drain, 0);
-    } else if (warp >= 2 && p.claim != nullptr) {
+    } else if ((warp == 2 || (!kConfirm && warp == 3)) && p.claim != nullptr) {
       // ===================== row gathers ====================================
       const int tid = threadIdx.x - 64;
       volatile int *bcast = reinterpret_cast<volatile int *>(&misc[5]);
       if (bh >= p.lookahead) {
         // slices of this CTA's own head that nobody has claimed yet
         for (;;) {
-          const int s = claim_slice(p.claim + bh, bcast, tid);
+          const int s = claim_slice<kGatherThreads>(p.claim + bh, bcast, tid);
           if (s >= p.nslices) break;
-          gather_slice<D>(p, bh, s, tid);
-          publish_slice(p.done + bh, tid);
+          gather_slice<D, kGatherThreads>(p, bh, s, tid);
+          publish_slice<kGatherThreads>(p.done + bh, tid);
         }
       }
       // one slice of a later head, ahead of time
       const int hp = bh + p.lookahead;
       if (hp < p.bh_total) {
-        const int s = claim_slice(p.claim + hp, bcast, tid);
+        const int s = claim_slice<kGatherThreads>(p.claim + hp, bcast, tid);
         if (s < p.nslices) {
-          gather_slice<D>(p, hp, s, tid);
-          publish_slice(p.done + hp, tid);
+          gather_slice<D, kGatherThreads>(p, hp, s, tid);
+          publish_slice<kGatherThreads>(p.done + hp, tid);
+        }
+      }
+    } else if (kConfirm && warp == 3 && lane == 0 && nmax > 0) {
+      // ===================== stage confirmer ================================
+      // Replays the MMA thread's order of slot takes; for each tile and
+      // iteration j it waits for the copies of the slots PV_t(j) and S_t(j+1)
+      // read (V_t(j), K_t(j+1)) and adds the last arrival the tile's P-ready
+      // barrier needs, so the MMA thread waits on P-ready alone.  Slots both
+      // tiles share are taken (and confirmed) by tile 0, whose group the MMA
+      // thread issues first.  It arrives for iteration j only after the
+      // barrier's phase of iteration j - 1 has completed.
+      int taken = (n_common > 0) ? 1 : ((n_t[0] > 0) + (n_t[1] > 0));  // prologue takes (K_t(0))
+      bool ok = true;
+      for (int j = 0; ok && j < nmax; ++j) {
+        int i = taken;
+        const int v0 = (j < n_t[0]) ? i++ : -1;
+        const int k0 = (j + 1 < n_t[0]) ? i++ : -1;
+        const int v1 = (j < n_t[1] && j >= n_common) ? i++ : -1;
+        const int k1 = (j + 1 < n_t[1] && j + 1 >= n_common) ? i++ : -1;
+        taken = i;
+        for (int t = 0; ok && t < kTiles; ++t) {
+          if (j >= n_t[t]) continue;
+          const int a = t == 0 ? v0 : v1, b = t == 0 ? k0 : k1;
+          if (a >= 0) ok = mbar_wait(&slot_full[a % S], (a / S) & 1, kSiteKFull, abort_flag);
+          if (ok && b >= 0) ok = mbar_wait(&slot_full[b % S], (b / S) & 1, kSiteKFull, abort_flag);
+          if (ok && j > 0) ok = mbar_wait(&p_full[t], (j - 1) & 1, kSitePFull, abort_flag);
+          if (ok) mbar_arrive(&p_full[t]);
         }
       }
     }
@@ -969,9 +1037,10 @@ cudaError_t run_attention(const AttnArgs &a, cudaStream_t st) {
 }
 
 // The dense kernel with the second K/V copy of every CTA (V_0) never issued:
-// the MMA thread's bounded wait for it gives up after `limit_ns` and records
-// kSiteKFull; every role unwinds (copies and MMAs drained, tensor memory
-// freed, nothing written).
+// the softmax withholds P-ready until that copy lands, so the MMA thread's
+// bounded wait for P gives up after `limit_ns` and records kSitePFull; every
+// role unwinds (copies and MMAs drained, tensor memory freed, nothing
+// written).
 cudaError_t run_attention_stall(const AttnArgs &a, uint64_t limit_ns, cudaStream_t st) {
   return run_attention_impl(a, st, limit_ns, 1);
 }

@@ -355,13 +355,14 @@ int ba_selftest_wait_timeout(uint32_t limit_us, ba_stream_t stream);
  * ba_selftest_attn_stall: exercises the attention kernel's own failure path
  * (BA-Att paper Algorithm 1 step 12 is the kernel under test) without a GPU
  * fault.  Runs ba_attn_dense on the caller's buffers with one change: the
- * second K/V copy of every CTA (the first V block) is never issued, so the
- * MMA-issuing thread's bounded wait for it runs out after limit_us
- * microseconds and records site 2 in the device error word.  Every role of
+ * second K/V copy of every CTA (the first V block) is never issued.  The
+ * softmax gives its first P-ready signal only once that copy has landed, so
+ * the MMA-issuing thread's bounded wait for it runs out after limit_us
+ * microseconds and records site 7 in the device error word.  Every role of
  * the CTA then unwinds: the copies and MMAs it issued complete, its tensor
  * memory is freed, and no O or LSE element is written.  A following
  * ba_last_device_error() returns BA_ERR_DEVICE_TIMEOUT with detail
- * (2 << 8) | 1 and clears the word; the context stays usable.
+ * (7 << 8) | 1 and clears the word; the context stays usable.
  *   q, k, v, o, lse, shape: as in ba_attn_dense; seqlen must exceed 128 (two
  *              key blocks), else BA_ERR_INVALID_ARG.
  *   limit_us   1 .. 1000000, else BA_ERR_INVALID_ARG.

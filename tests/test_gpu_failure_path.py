@@ -49,14 +49,14 @@ def test_context_usable_after_a_timeout(dev):
     check_attention(to64(o), lse.cpu().double().numpy(), o_ref, lse_ref)
 
 
-SITE_K_FULL = 2  # the MMA thread's wait for a K/V copy that is never issued
+SITE_P_FULL = 7  # the MMA thread's wait for P-ready, held back by a K/V copy never issued
 
 
 def test_attention_kernel_unwinds_after_a_stalled_stage(dev):
     """The attention kernel's own bounded wait runs out (its MMA thread waits
-    for a K/V copy that is never issued): the site is reported, nothing is
-    written, the word clears, and the next select + attention matches the
-    oracle."""
+    for a P-ready signal that a K/V copy which is never issued holds back):
+    the site is reported, nothing is written, the word clears, and the next
+    select + attention matches the oracle."""
     assert bsb.last_device_error() == (0, 0)
     q, k, v = workloads.random_inputs(1, 2, 1024, 128, seed=5)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -65,7 +65,7 @@ def test_attention_kernel_unwinds_after_a_stalled_stage(dev):
     bsb.selftest_attn_stall(qd, kd, vd, o, lse, limit_us=1000)
     st, word = bsb.last_device_error()
     assert st == DEVICE_TIMEOUT
-    assert word & 1 and (word >> 8) & 0xFF == SITE_K_FULL
+    assert word & 1 and (word >> 8) & 0xFF == SITE_P_FULL
     assert bsb.last_device_error() == (0, 0)
     # an aborted CTA writes no output
     assert bool((o == 7.0).all()) and bool((lse == 7.0).all())
