@@ -146,39 +146,81 @@ struct AttnParams {
 // (k_pair_lists); dense tiles walk every block.
 __device__ __forceinline__ uint32_t dense_entry(int j) { return static_cast<uint32_t>(j) | (3u << 12); }
 
-// One CTA's share of the row gathers of head hp (kGatherThreads threads,
-// 16 bytes each per access; 16 rows of the slice in flight per pass).
-template <int D, int kGatherThreads>
-__device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pair, int tid) {
-  constexpr int kGatherUnroll = kGatherThreads == 32 ? 8 : 4;
+// Copies rows [r_begin, r_end) of one head through a permutation into the
+// gathered layout, for one tensor (s1 == nullptr) or for two that share it
+// (K and V).  A thread owns 16 bytes of kU rows per step.  While a step's
+// rows are in flight the thread loads the next step's permutation entries
+// and asks L2 for the next step's rows (prefetches hold no register), and
+// the entries two steps ahead are prefetched too, so a step mostly waits
+// for L2, not for an index load followed by a DRAM row load.
+template <int D, int kGatherThreads, int kU>
+__device__ __forceinline__ void copy_rows(const __nv_bfloat16 *s0, const __nv_bfloat16 *s1,
+                                          __nv_bfloat16 *d0, __nv_bfloat16 *d1, const int32_t *perm,
+                                          int r_begin, int r_end, int L, int tid) {
   constexpr int VPR = D / 8;                 // 16-byte pieces per row
   constexpr int RPP = kGatherThreads / VPR;  // rows per pass of the gather threads
-  const int c = tid % VPR, rsub = tid / VPR;
-  const int64_t base = static_cast<int64_t>(hp) * p.L;
-  const int r_begin = pair * p.slice_rows;
-  const int r_end = min(p.L, r_begin + p.slice_rows);
-  for (int op = 0; op < 3; ++op) {
-    const __nv_bfloat16 *src = op == 0 ? p.src_q : (op == 1 ? p.src_k : p.src_v);
-    __nv_bfloat16 *dst = op == 0 ? p.dst_q : (op == 1 ? p.dst_k : p.dst_v);
-    const int32_t *perm = op == 0 ? p.perm_q : p.perm_k;
-    if (dst == nullptr) continue;
-    for (int r0 = r_begin; r0 < r_end; r0 += RPP * kGatherUnroll) {
-      uint4 v[kGatherUnroll];
+  constexpr int kStep = RPP * kU;
+  const int c = tid % VPR;
+  const int rs = r_begin + tid / VPR;
+  // pointers of this head and piece; row offsets fit 32 bits (L * D < 2^31)
+  const uint4 *x0 = reinterpret_cast<const uint4 *>(s0) + c;
+  const uint4 *x1 = reinterpret_cast<const uint4 *>(s1) + c;
+  uint4 *y0 = reinterpret_cast<uint4 *>(d0) + c;
+  uint4 *y1 = reinterpret_cast<uint4 *>(d1) + c;
+  int src[kU];
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int row = r0 + u * RPP + rsub;
-        if (row < r_end) {
-          const int64_t s = base + min(max(__ldg(perm + base + row), 0), p.L - 1);
-          v[u] = __ldg(reinterpret_cast<const uint4 *>(src + s * D) + c);
-        }
+  for (int u = 0; u < kU; ++u) {
+    const int row = rs + u * RPP;
+    src[u] = (row < r_end) ? min(max(__ldg(perm + row), 0), L - 1) : 0;
+  }
+  for (int r0 = rs; r0 < r_end; r0 += kStep) {
+    uint4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (r0 + u * RPP < r_end) {
+        a[u] = __ldg(x0 + src[u] * VPR);
+        if (s1 != nullptr) b[u] = __ldg(x1 + src[u] * VPR);
       }
+    }
 #pragma unroll
-      for (int u = 0; u < kGatherUnroll; ++u) {
-        const int row = r0 + u * RPP + rsub;
-        if (row < r_end) reinterpret_cast<uint4 *>(dst + (base + row) * D)[c] = v[u];
+    for (int u = 0; u < kU; ++u) {  // the next step's indices, in flight with the rows
+      const int row = r0 + kStep + u * RPP;
+      src[u] = (row < r_end) ? min(max(__ldg(perm + row), 0), L - 1) : 0;
+    }
+    if (c == 0 && r0 + 2 * kStep < r_end) prefetch_l2(perm + r0 + 2 * kStep);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (r0 + kStep + u * RPP < r_end) {
+        prefetch_l2(x0 + src[u] * VPR);
+        if (s1 != nullptr) prefetch_l2(x1 + src[u] * VPR);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int row = r0 + u * RPP;
+      if (row < r_end) {
+        y0[row * VPR] = a[u];
+        if (s1 != nullptr) y1[row * VPR] = b[u];
       }
     }
   }
+}
+
+// One CTA's share of the row gathers of head hp: slice `pair` of Q' (through
+// pi_q) and of K' and V' (through pi_k, one index load for both rows).
+template <int D, int kGatherThreads>
+__device__ __forceinline__ void gather_slice(const AttnParams &p, int hp, int pair, int tid) {
+  const int64_t base = static_cast<int64_t>(hp) * p.L;
+  const int64_t xb = base * D;
+  const int r_begin = pair * p.slice_rows;
+  const int r_end = min(p.L, r_begin + p.slice_rows);
+  if (p.dst_q != nullptr)
+    copy_rows<D, kGatherThreads, 2>(p.src_q + xb, nullptr, p.dst_q + xb, nullptr, p.perm_q + base, r_begin,
+                                    r_end, p.L, tid);
+  if (p.dst_k != nullptr)
+    copy_rows<D, kGatherThreads, 2>(p.src_k + xb, p.dst_v != nullptr ? p.src_v + xb : nullptr, p.dst_k + xb,
+                                    p.dst_v != nullptr ? p.dst_v + xb : nullptr, p.perm_k + base, r_begin, r_end,
+                                    p.L, tid);
 }
 
 // Gathers run on kGatherThreads threads (one warp, or warps 2-3): a named
@@ -889,6 +931,23 @@ static int gather_lookahead(int npairs) {
   return (2 * sms + npairs - 1) / npairs;
 }
 
+// The in-kernel copies pay while a CTA's own attention work outlasts its
+// share of them (one slice of a later head: 2 x 128 rows of each gathered
+// tensor, read and written).  Measured on GB300 (d = 128, two 128-row tiles
+// per CTA): a key-slot iteration takes ~1.7 us; one gather warp copies a
+// CTA's share of Q', K' and V' in ~75 us, the packed kernel's two warps in
+// about half that.  A 128-token-block CTA walks ~kappa slots, a 64-token one
+// ~kappa / 2 (two entries per slot).  Both sides scale alike with d.  Below
+// the balance (L = 32768 at 90% sparsity: kappa 26, 2.02 ms with the copies
+// in the kernel) every head is gathered by the separate pass instead.
+static bool gathers_hide_under_attention(int kappa, int BK, int njobs) {
+  const int64_t slots = BK == 128 ? kappa : (kappa + 1) / 2;
+  const int64_t warps = BK == 128 ? 1 : 2;
+  const int64_t attn_tenths_us = slots * 17;
+  const int64_t copy_tenths_us = 750 * njobs / (3 * warps);
+  return attn_tenths_us >= copy_tenths_us;
+}
+
 template <int D, int BK, bool kDense, bool kPack = false>
 static cudaError_t launch_attn(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                                const AttnParams &p, int64_t bh, cudaStream_t st) {
@@ -954,7 +1013,8 @@ static cudaError_t run_attention_impl(const AttnArgs &a, cudaStream_t st, uint64
   // attention kernel, the others inside it (claimed slices).
   int *counters = nullptr;
   const int lookahead = gather_lookahead(npairs);
-  const bool in_kernel_gathers = !dense && njobs > 0 && lookahead < bh;
+  const bool in_kernel_gathers =
+      !dense && njobs > 0 && lookahead < bh && gathers_hide_under_attention(a.kappa, BK, njobs);
   if (!dense) {
     const int64_t nblk = (L + BK - 1) / BK;
     pair_lists = reinterpret_cast<uint16_t *>(ws);

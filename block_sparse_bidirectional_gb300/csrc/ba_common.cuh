@@ -159,6 +159,11 @@ __device__ __forceinline__ bool wait_counter_at_least(const int *counter, int ta
   return ok;
 }
 
+// Brings the line holding `ptr` into L2 without a register destination.
+__device__ __forceinline__ void prefetch_l2(const void *ptr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

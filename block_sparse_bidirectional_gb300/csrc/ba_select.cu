@@ -5,13 +5,16 @@
 //   k_sqnorm_keys   Eq. 9: fp32 squared norm of every Q / K row, packed with
 //                   the token index into a 64-bit sort key.  One streaming
 //                   pass over Q and K (16-byte vector loads, coalesced).
-//   k_chunk_sort    Eq. 10: 4096-key chunks: each thread sorts 8 keys in
-//                   registers (a 19-comparator network), the CTA merges the
-//                   runs in shared memory (merge path, 9 levels).
-//   k_merge_pass    merge-path merge of sorted runs (width doubles per pass);
-//                   the last pass emits pi (sorted position -> token index).
-//                   Keys are unique (index in the low word), so the result is
-//                   the stable sort.
+//   k_chunk_sort    Eq. 10, windows of up to 4096 keys: each thread sorts 8
+//                   keys in registers (a 19-comparator network), the CTA
+//                   merges the runs in shared memory (merge path, 9 levels)
+//                   and emits pi (sorted position -> token index).  Keys are
+//                   unique (index in the low word), so the result is the
+//                   stable sort.
+//   k_radix_pass    Eq. 10, longer windows: four stable 8-bit LSD radix
+//                   passes over the norm bits, one cluster of 4 CTAs per
+//                   window exchanging digit totals through distributed
+//                   shared memory; the last pass emits pi.
 //   k_block_stats   Algorithm 1 step 4: gathers the rows of sorted blocks
 //                   through pi into shared memory (cp.async, double-buffered
 //                   across the blocks a CTA walks); two-pass fp32 mean and
@@ -43,8 +46,6 @@ namespace ba {
 
 constexpr int kChunk = 4096;          // keys sorted per CTA (16 warps x 256)
 constexpr int kSortThreads = 512;
-constexpr int kMergeThreads = 256;
-constexpr int kMergeItems = 8;        // outputs per merge thread
 constexpr int kStatsThreads = 256;
 constexpr int kTopkWarps = 4;
 constexpr int kNormRowsPerThread = 4;
@@ -93,10 +94,11 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
 }
 
 // ---------------------------------------------------------------------------
-// step 1-2b: chunk sort.  grid = (chunks per window, windows, sorted sequences)
-// A thread sorts its 8 consecutive keys in registers; the CTA then merges
-// the 512 runs in shared memory (merge path, 9 levels).  Keys are unique,
-// so the order is the stable one.
+// step 1-2, windows of up to kChunk keys: one CTA per window.
+// grid = (1, windows, sorted sequences).  A thread sorts its 8 consecutive
+// keys in registers; the CTA then merges the 512 runs in shared memory
+// (merge path, 9 levels) and writes pi.  Keys are unique, so the order is
+// the stable one.
 // ---------------------------------------------------------------------------
 struct SortGeom {
   int L;        // tokens per sequence
@@ -115,25 +117,6 @@ __device__ __forceinline__ int window_len(const SortGeom &g, int w) {
   if (g.split > 0) return w == 0 ? g.split : g.L - g.split;
   const int start = w * g.win;
   return min(g.win, g.L - start);
-}
-
-__device__ __forceinline__ void merge_path_8(const uint64_t *A, const uint64_t *B, int la, int lb,
-                                             int diag, int n, uint64_t *dst) {
-  int lo = max(0, diag - lb), hi = min(diag, la);
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (A[mid] < B[diag - 1 - mid])
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  int i = lo, j = diag - lo;
-  for (int t = 0; t < n; ++t) {
-    if (i < la && (j >= lb || A[i] < B[j]))
-      dst[t] = A[i++];
-    else
-      dst[t] = B[j++];
-  }
 }
 
 // Shared-memory arrays of 64-bit keys are padded with one word per 8 so that
@@ -171,10 +154,8 @@ __device__ __forceinline__ void merge_path_8_smem(const uint64_t *s, int a0, int
 }
 
 __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__restrict__ keys_in,
-                                                             uint64_t *__restrict__ keys_out,
                                                              int32_t *__restrict__ perm0,
-                                                             int32_t *__restrict__ perm1,
-                                                             SortGeom g, int final_pass) {
+                                                             int32_t *__restrict__ perm1, SortGeom g) {
   extern __shared__ __align__(16) uint64_t sbuf[];  // 2 x padded kChunk
   uint64_t *sa = sbuf, *sb = sbuf + spad_size(kChunk);
   const int w = blockIdx.y;
@@ -218,98 +199,8 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
   }
   int32_t *perm = (seq < g.bh) ? perm0 : perm1;
   const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w) + c0;
-  for (int i = threadIdx.x; i < n; i += kSortThreads) {
-    if (final_pass)
-      perm[pbase + i] = static_cast<int32_t>(src[spad(i)] & 0xffffffffu);
-    else
-      keys_out[base + i] = src[spad(i)];
-  }
-}
-
-// ---------------------------------------------------------------------------
-// step 1-2c: merge pass.  Runs of `width` inside each window are merged in
-// pairs.  grid = (ceil(win / (threads*items)), windows, sorted sequences)
-// ---------------------------------------------------------------------------
-// Each CTA produces kMergeTile consecutive outputs of one merged pair: one
-// merge-path split per CTA boundary, the two input ranges staged in shared
-// memory with coalesced loads, per-thread merges of kMergeItems from shared
-// memory, coalesced stores.
-constexpr int kMergeTile = kMergeThreads * kMergeItems;
-
-__global__ void __launch_bounds__(kMergeThreads) k_merge_pass(const uint64_t *__restrict__ in,
-                                                              uint64_t *__restrict__ out,
-                                                              int32_t *__restrict__ perm0,
-                                                              int32_t *__restrict__ perm1,
-                                                              SortGeom g, int width,
-                                                              int final_pass) {
-  __shared__ uint64_t s_in[spad_size(kMergeTile)];
-  __shared__ uint64_t s_out[spad_size(kMergeTile)];
-  __shared__ int s_lo[2], s_hi[2], s_cnt[2];
-  const int w = blockIdx.y;
-  const int seq = blockIdx.z;
-  const int wlen = window_len(g, w);
-  const int o_cta = blockIdx.x * kMergeTile;
-  if (o_cta >= wlen) return;  // uniform over the CTA
-  const int64_t base = static_cast<int64_t>(seq) * g.L + window_start(g, w);
-  const int p0 = (o_cta / (2 * width)) * 2 * width;
-  const int a1 = min(p0 + width, wlen), b1 = min(p0 + 2 * width, wlen);
-  const int la = a1 - p0, lb = b1 - a1;
-  const uint64_t *A = in + base + p0;
-  const uint64_t *B = in + base + a1;
-  const int d0 = o_cta - p0;
-  const int cnt = min(kMergeTile, la + lb - d0);
-  // The merge-path splits of this CTA's first and one-past-last outputs:
-  // ans = #A elements among the first `diag` outputs, the first i in
-  // [lo, hi] with !(A[i] < B[diag-1-i]).  Each half of the CTA narrows one
-  // split by probing 128 evenly spaced candidates per round (a span of
-  // 2^15 resolves in 3 rounds instead of 15 dependent probes).
-  constexpr int kGroup = kMergeThreads / 2;
-  const int grp = threadIdx.x / kGroup, u = threadIdx.x % kGroup;
-  const int diag = d0 + (grp == 0 ? 0 : cnt);
-  if (u == 0) {
-    s_lo[grp] = max(0, diag - lb);
-    s_hi[grp] = min(diag, la);
-  }
-  __syncthreads();
-  for (int round = 0; round < 8; ++round) {
-    const int lo = s_lo[grp], hi = s_hi[grp];
-    const bool active = s_hi[0] > s_lo[0] || s_hi[1] > s_lo[1];  // uniform
-    __syncthreads();
-    if (!active) break;
-    if (u == 0) s_cnt[grp] = 0;
-    __syncthreads();
-    const int span = hi - lo;
-    const int step = (span + kGroup - 1) / kGroup;
-    const int i = lo + u * step;
-    const bool t = span > 0 && i < hi && A[i] < B[diag - 1 - i];
-    const uint32_t bal = __ballot_sync(0xffffffffu, t);
-    if ((threadIdx.x & 31) == 0 && bal) atomicAdd(&s_cnt[grp], __popc(bal));
-    __syncthreads();
-    if (u == 0 && span > 0) {
-      const int c = s_cnt[grp];
-      s_lo[grp] = (c > 0) ? lo + (c - 1) * step + 1 : lo;
-      s_hi[grp] = min(hi, lo + c * step);
-    }
-    __syncthreads();
-  }
-  const int ia0 = s_lo[0], ia1 = s_lo[1];
-  const int ib0 = d0 - ia0, ib1 = d0 + cnt - ia1;
-  const int na = ia1 - ia0, nb = ib1 - ib0;  // na + nb == cnt
-  for (int i = threadIdx.x; i < na; i += kMergeThreads) s_in[spad(i)] = A[ia0 + i];
-  for (int i = threadIdx.x; i < nb; i += kMergeThreads) s_in[spad(na + i)] = B[ib0 + i];
-  __syncthreads();
-  const int t0 = threadIdx.x * kMergeItems;
-  if (t0 < cnt)
-    merge_path_8_smem(s_in, 0, na, na, nb, t0, min(kMergeItems, cnt - t0), s_out, t0);
-  __syncthreads();
-  int32_t *perm = (seq < g.bh) ? perm0 : perm1;
-  const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w);
-  for (int i = threadIdx.x; i < cnt; i += kMergeThreads) {
-    if (final_pass)
-      perm[pbase + o_cta + i] = static_cast<int32_t>(s_out[spad(i)] & 0xffffffffu);
-    else
-      out[base + o_cta + i] = s_out[spad(i)];
-  }
+  for (int i = threadIdx.x; i < n; i += kSortThreads)
+    perm[pbase + i] = static_cast<int32_t>(src[spad(i)] & 0xffffffffu);
 }
 
 // ---------------------------------------------------------------------------
@@ -937,9 +828,7 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
     }
     return cudaSuccess;
   }
-  int npasses = 0;
-  for (int w = kChunk; w < g.win; w <<= 1) ++npasses;
-  const int chunks = (g.win + kChunk - 1) / kChunk;
+  // one chunk covers the window: keys -> pi
   const size_t smem = 2 * spad_size(kChunk) * sizeof(uint64_t);
   static std::atomic<uint64_t> configured{0};
   e = once_per_device(configured, [smem] {
@@ -947,25 +836,8 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
                                 static_cast<int>(smem));
   });
   if (e != cudaSuccess) return e;
-  // chunk sort: keys -> buf0 (or pi when no merge pass follows)
-  k_chunk_sort<<<dim3(chunks, g.nwin, nseq), kSortThreads, smem, st>>>(keys, buf0, perm0, perm1,
-                                                                        g, npasses == 0);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const uint64_t *src = buf0;
-  uint64_t *dst = buf1;
-  int width = kChunk;
-  for (int p = 0; p < npasses; ++p) {
-    const int per_cta = kMergeThreads * kMergeItems;
-    const int gx = (g.win + per_cta - 1) / per_cta;
-    k_merge_pass<<<dim3(gx, g.nwin, nseq), kMergeThreads, 0, st>>>(src, dst, perm0, perm1, g,
-                                                                   width, p == npasses - 1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const uint64_t *t = dst;
-    dst = const_cast<uint64_t *>(src);
-    src = t;
-    width <<= 1;
-  }
-  return cudaSuccess;
+  k_chunk_sort<<<dim3(1, g.nwin, nseq), kSortThreads, smem, st>>>(keys, perm0, perm1, g);
+  return cudaGetLastError();
 }
 
 template <int D, int BK>
