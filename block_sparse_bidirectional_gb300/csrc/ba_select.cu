@@ -213,7 +213,9 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
 // one lane per digit adds); the CTAs exchange their digit totals through
 // distributed shared memory; each (warp, digit) gets its first output
 // position; a second sweep writes every key at that position plus its rank
-// among the equal digits of its 32-key chunk.  Equal norms keep the input
+// among the equal digits of the warp's slice (kept from the first sweep for
+// parts that fit the shared-memory stage, else recounted per 32-key chunk).
+// Equal norms keep the input
 // (token index) order, the order the keys start in.  The last pass writes pi.
 // grid = (kRadixCluster * windows, sorted sequences)
 // ---------------------------------------------------------------------------
@@ -228,8 +230,8 @@ constexpr int kRadixBins = 256;
 // their keys and scatter them directly.
 constexpr int kRadixRegChunks = 16;
 constexpr int kRadixStage = kRadixWarps * kRadixRegChunks * 32;
-constexpr size_t kRadixSmem =
-    sizeof(int) * (kRadixWarps * kRadixBins + 3 * kRadixBins + kRadixBins / 32) + sizeof(uint64_t) * kRadixStage;
+constexpr size_t kRadixSmem = sizeof(int) * (kRadixWarps * kRadixBins + 3 * kRadixBins + kRadixBins / 32) +
+                              sizeof(uint64_t) * kRadixStage + sizeof(uint16_t) * kRadixStage;
 
 __global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixThreads)
     k_radix_pass(const uint64_t *__restrict__ in, uint64_t *__restrict__ out, int32_t *__restrict__ perm0,
@@ -242,6 +244,8 @@ __global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixTh
   int *lbase = total + kRadixBins;      // first staged position of each digit
   int *delta = lbase + kRadixBins;      // output position - staged position, per digit
   int *wsum = delta + kRadixBins;       // [kRadixBins / 32]
+  // staged parts: each key's rank among the equal digits of its warp's slice
+  uint16_t *lrank = reinterpret_cast<uint16_t *>(wsum + kRadixBins / 32);  // [kRadixStage]
   cg::cluster_group cluster = cg::this_cluster();
   const int r = static_cast<int>(cluster.block_rank());
   const int w = blockIdx.x / kRadixCluster;
@@ -257,6 +261,7 @@ __global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixTh
   // uniform over the cluster (all its parts differ in length by at most one)
   const bool staged = (wlen + kRadixCluster - 1) / kRadixCluster <= kRadixStage;
   const uint32_t lt_mask = (1u << lane) - 1u;
+  uint16_t *lrank_w = lrank + (s0 - p0);  // this warp's slice of the ranks
   auto digit = [&](uint64_t key) { return static_cast<int>((key >> (32 + shift)) & 0xFFu); };
   // lanes of `m` whose digit equals this lane's: eight ballots, one per
   // digit bit (a constant cost, whatever the number of distinct digits;
@@ -291,9 +296,12 @@ __global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixTh
       if (act) {
         const int dig = digit(kr[u]);
         const uint32_t peers = same_digit(m, dig);
-        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
+        const int before = hist[warp][dig];
+        lrank_w[u * 32 + lane] = static_cast<uint16_t>(before + __popc(peers & lt_mask));
+        __syncwarp(m);  // every lane has read the count before its digit's leader updates it
+        if ((peers & lt_mask) == 0u) hist[warp][dig] = before + __popc(peers);
       }
-      __syncwarp();  // the next chunk's leader of a digit sees this update
+      __syncwarp();  // the next chunk's lanes see this update
     }
   } else {
     for (int c = s0; c < s1; c += 32) {
@@ -380,17 +388,8 @@ __global__ void __cluster_dims__(kRadixCluster, 1, 1) __launch_bounds__(kRadixTh
     for (int u = 0; u < kRadixRegChunks; ++u) {
       const int i = s0 + u * 32 + lane;
       if (s0 + u * 32 >= s1) break;
-      const bool act = i < s1;
-      const uint32_t m = __ballot_sync(0xffffffffu, act);
-      if (act) {
-        const int dig = digit(kr[u]);
-        const uint32_t peers = same_digit(m, dig);
-        const int dest = hist[warp][dig] + __popc(peers & lt_mask);
-        __syncwarp(m);
-        if ((peers & lt_mask) == 0u) hist[warp][dig] += __popc(peers);
-        stage[dest] = kr[u];
-      }
-      __syncwarp();
+      // the warp's first staged position of the digit plus the rank sweep 1 kept
+      if (i < s1) stage[hist[warp][digit(kr[u])] + lrank_w[u * 32 + lane]] = kr[u];
     }
     __syncthreads();
     const int n = p1 - p0;
