@@ -54,7 +54,7 @@ constexpr int kNormRowsPerThread = 4;
 // step 1-2a: squared norms -> sort keys.  grid = (.., sorted tensors)
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__restrict__ x0,
+__global__ void __launch_bounds__(256, 8) k_sqnorm_keys(const __nv_bfloat16 *__restrict__ x0,
                                                      const __nv_bfloat16 *__restrict__ x1,
                                                      uint64_t *__restrict__ keys, int64_t rows,
                                                      int L) {
@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
   uint64_t *out = keys + static_cast<int64_t>(blockIdx.y) * rows;
   const int part = threadIdx.x % TPR;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPW * kNormRowsPerThread + threadIdx.x / TPR;
+  // token index of row0 (rows of one thread are RPW apart)
+  int tok0 = static_cast<int>(row0 % L);
   uint4 raw[kNormRowsPerThread];
 #pragma unroll
   for (int u = 0; u < kNormRowsPerThread; ++u) {
@@ -86,10 +88,10 @@ __global__ void __launch_bounds__(256) k_sqnorm_keys(const __nv_bfloat16 *__rest
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     const int64_t row = row0 + u * RPW;
-    if (row < rows && part == 0) {
-      const uint32_t tok = static_cast<uint32_t>(row % L);
-      out[row] = (static_cast<uint64_t>(__float_as_uint(acc)) << 32) | tok;
-    }
+    if (row < rows && part == 0)
+      out[row] = (static_cast<uint64_t>(__float_as_uint(acc)) << 32) | static_cast<uint32_t>(tok0);
+    tok0 += RPW;
+    while (tok0 >= L) tok0 -= L;
   }
 }
 
