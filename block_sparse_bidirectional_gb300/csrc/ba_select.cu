@@ -496,11 +496,13 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
   // added in slice order by one thread
   const int quad = threadIdx.x % QPR, part = threadIdx.x / QPR;
   const int dim = threadIdx.x;  // feature owned in the combine step (< D)
-  auto load4 = [&](const __nv_bfloat16 *rows, int r, float (&f)[4]) {
+  // four features of row r as two packed fp32 pairs (a bf16 is the top half
+  // of its fp32), so the sums below run as f32x2 adds / fmas: the same IEEE
+  // operation per feature, half the instructions
+  auto load4 = [&](const __nv_bfloat16 *rows, int r, uint64_t &p01, uint64_t &p23) {
     const uint2 w = *reinterpret_cast<const uint2 *>(rows + r * D + quad * 4);
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
-    f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+    p01 = f2_pack(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+    p23 = f2_pack(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
   };
   for (int bi = 0; bi < nblk; ++bi) {
     if (bi + 1 < nblk) {
@@ -513,13 +515,16 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
     const __nv_bfloat16 *rows = stage[bi & 1];
     const int g = g0 + bi;
     const int n = min(BK, L - g * BK);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint64_t a01 = f2_pack(0.f, 0.f), a23 = a01;
     for (int r = part; r < n; r += P) {
-      float f[4];
-      load4(rows, r, f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c] += f[c];
+      uint64_t p01, p23;
+      load4(rows, r, p01, p23);
+      a01 = f2_add(a01, p01);
+      a23 = f2_add(a23, p23);
     }
+    float acc[4];
+    f2_unpack(a01, acc[0], acc[1]);
+    f2_unpack(a23, acc[2], acc[3]);
     *reinterpret_cast<float4 *>(&red[part][quad * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
     if (threadIdx.x < D) {
@@ -530,18 +535,18 @@ __global__ void __launch_bounds__(kStatsThreads) k_block_stats(
     }
     __syncthreads();
     const float4 m4 = *reinterpret_cast<const float4 *>(&s_mean[quad * 4]);
-    const float mq[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[c] = 0.f;
+    const uint64_t nm01 = f2_pack(-m4.x, -m4.y), nm23 = f2_pack(-m4.z, -m4.w);
+    a01 = f2_pack(0.f, 0.f);
+    a23 = a01;
     for (int r = part; r < n; r += P) {
-      float f[4];
-      load4(rows, r, f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float dv = f[c] - mq[c];
-        acc[c] = fmaf(dv, dv, acc[c]);
-      }
+      uint64_t p01, p23;
+      load4(rows, r, p01, p23);
+      const uint64_t d01 = f2_add(p01, nm01), d23 = f2_add(p23, nm23);  // x - mean
+      a01 = f2_fma(d01, d01, a01);
+      a23 = f2_fma(d23, d23, a23);
     }
+    f2_unpack(a01, acc[0], acc[1]);
+    f2_unpack(a23, acc[2], acc[3]);
     *reinterpret_cast<float4 *>(&red[part][quad * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     __syncthreads();
     if (threadIdx.x < D) {
