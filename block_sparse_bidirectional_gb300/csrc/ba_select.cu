@@ -5,7 +5,7 @@
 //   k_sqnorm_keys   Eq. 9: fp32 squared norm of every Q / K row, packed with
 //                   the token index into a 64-bit sort key.  One streaming
 //                   pass over Q and K (16-byte vector loads, coalesced).
-//   k_chunk_sort    Eq. 10, windows of up to 4096 keys: each thread sorts 8
+//   k_chunk_sort    Eq. 10, windows of up to 8192 keys: each thread sorts 8
 //                   keys in registers (a 19-comparator network), the CTA
 //                   merges the runs in shared memory (merge path, 9 levels)
 //                   and emits pi (sorted position -> token index).  Keys are
@@ -44,8 +44,9 @@
 
 namespace ba {
 
-constexpr int kChunk = 4096;          // keys sorted per CTA (16 warps x 256)
-constexpr int kSortThreads = 512;
+// Windows of up to kChunkMax keys are sorted by one CTA (k_chunk_sort, 8 keys
+// per thread, 512 or 1024 threads); longer ones by the clustered radix sort.
+constexpr int kChunkMax = 8192;
 constexpr int kStatsThreads = 256;
 constexpr int kTopkWarps = 4;
 constexpr int kNormRowsPerThread = 4;
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(256, 8) k_sqnorm_keys(const __nv_bfloat16 *__r
 }
 
 // ---------------------------------------------------------------------------
-// step 1-2, windows of up to kChunk keys: one CTA per window.
+// step 1-2, windows of up to kChunkMax keys: one CTA per window.
 // grid = (1, windows, sorted sequences).  A thread sorts its 8 consecutive
 // keys in registers; the CTA then merges the 512 runs in shared memory
 // (merge path, 9 levels) and writes pi.  Keys are unique, so the order is
@@ -155,9 +156,11 @@ __device__ __forceinline__ void merge_path_8_smem(const uint64_t *s, int a0, int
   }
 }
 
-__global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__restrict__ keys_in,
-                                                             int32_t *__restrict__ perm0,
-                                                             int32_t *__restrict__ perm1, SortGeom g) {
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) k_chunk_sort(const uint64_t *__restrict__ keys_in,
+                                                         int32_t *__restrict__ perm0,
+                                                         int32_t *__restrict__ perm1, SortGeom g) {
+  constexpr int kChunk = 8 * kThreads;  // keys per CTA
   extern __shared__ __align__(16) uint64_t sbuf[];  // 2 x padded kChunk
   uint64_t *sa = sbuf, *sb = sbuf + spad_size(kChunk);
   const int w = blockIdx.y;
@@ -188,7 +191,7 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
   for (int i = 0; i < 8; ++i) sa[spad(e0 + i)] = r[i];
   __syncthreads();
 
-  // ---- merge the 512 sorted runs: 8 -> 16 -> ... -> 4096 ----
+  // ---- merge the kThreads sorted runs: 8 -> 16 -> ... -> kChunk ----
   uint64_t *src = sa, *dst = sb;
   for (int width = 8; width < kChunk; width <<= 1) {
     const int o0 = threadIdx.x * 8;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kSortThreads) k_chunk_sort(const uint64_t *__r
   }
   int32_t *perm = (seq < g.bh) ? perm0 : perm1;
   const int64_t pbase = static_cast<int64_t>(seq % g.bh) * g.L + window_start(g, w) + c0;
-  for (int i = threadIdx.x; i < n; i += kSortThreads)
+  for (int i = threadIdx.x; i < n; i += kThreads)
     perm[pbase + i] = static_cast<int32_t>(src[spad(i)] & 0xffffffffu);
 }
 
@@ -612,13 +615,25 @@ __global__ void __launch_bounds__(256) k_scores(const float *__restrict__ A,
   const float *brow = Bb + (j0 + lr) * static_cast<int64_t>(stride) + lk;
   const bool a_ok = load_a && i0 + lr < N, b_ok = load_b && j0 + lr < N;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 na4 = a_ok ? *reinterpret_cast<const float4 *>(arow) : z4;
-  float4 nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow) : z4;
-  for (int k0 = 0; k0 < KS; k0 += BKK) {
-    const float4 va = na4, vb = nb4;
-    if (k0 + BKK < KS) {  // prefetch the next chunk while this one is used
-      na4 = a_ok ? *reinterpret_cast<const float4 *>(arow + k0 + BKK) : z4;
-      nb4 = b_ok ? *reinterpret_cast<const float4 *>(brow + k0 + BKK) : z4;
+  // kPF k-chunks in flight (registers): a CTA's chunks are a chain of L2
+  // round trips, and the 64-wide tiles serve short grids with few CTAs to
+  // hide them (the 128-wide tiles keep one: more would cost them their
+  // second CTA per SM); KS / BKK (8, 16, 24 or 48) is a multiple of kPF
+  constexpr int kPF = TM == 64 ? 4 : 1;
+  float4 na4[kPF], nb4[kPF];
+#pragma unroll
+  for (int u = 0; u < kPF; ++u) {
+    na4[u] = (a_ok && u * BKK < KS) ? *reinterpret_cast<const float4 *>(arow + u * BKK) : z4;
+    nb4[u] = (b_ok && u * BKK < KS) ? *reinterpret_cast<const float4 *>(brow + u * BKK) : z4;
+  }
+  for (int k00 = 0; k00 < KS; k00 += kPF * BKK)
+#pragma unroll
+  for (int u = 0; u < kPF; ++u) {
+    const int k0 = k00 + u * BKK;
+    const float4 va = na4[u], vb = nb4[u];
+    if (k0 + kPF * BKK < KS) {  // the chunk kPF ahead replaces this one
+      na4[u] = a_ok ? *reinterpret_cast<const float4 *>(arow + k0 + kPF * BKK) : z4;
+      nb4[u] = b_ok ? *reinterpret_cast<const float4 *>(brow + k0 + kPF * BKK) : z4;
     }
     if (load_a) {
       As[lk + 0][lr] = va.x; As[lk + 1][lr] = va.y; As[lk + 2][lr] = va.z; As[lk + 3][lr] = va.w;
@@ -815,7 +830,7 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
     g.nwin = (L + g.win - 1) / g.win;
   }
   cudaError_t e;
-  if (g.win > kChunk) {
+  if (g.win > kChunkMax) {
     // long windows: four radix passes, keys -> buf0 -> buf1 -> buf0 -> pi
     static std::atomic<uint64_t> radix_configured{0};
     e = once_per_device(radix_configured, [] {
@@ -834,15 +849,24 @@ static cudaError_t sort_sequences(const uint64_t *keys, uint64_t *buf0, uint64_t
     }
     return cudaSuccess;
   }
-  // one chunk covers the window: keys -> pi
-  const size_t smem = 2 * spad_size(kChunk) * sizeof(uint64_t);
+  // one CTA covers the window: keys -> pi (4096 keys with 512 threads, up to
+  // 8192 with 1024: at L = 8192 one launch instead of four radix passes whose
+  // parts of 2048 keys are dominated by the cluster exchanges)
   static std::atomic<uint64_t> configured{0};
-  e = once_per_device(configured, [smem] {
-    return cudaFuncSetAttribute(k_chunk_sort, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(smem));
+  e = once_per_device(configured, [] {
+    cudaError_t r = cudaFuncSetAttribute(k_chunk_sort<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(2 * spad_size(4096) * sizeof(uint64_t)));
+    if (r != cudaSuccess) return r;
+    return cudaFuncSetAttribute(k_chunk_sort<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(2 * spad_size(8192) * sizeof(uint64_t)));
   });
   if (e != cudaSuccess) return e;
-  k_chunk_sort<<<dim3(1, g.nwin, nseq), kSortThreads, smem, st>>>(keys, perm0, perm1, g);
+  if (g.win <= 4096)
+    k_chunk_sort<512><<<dim3(1, g.nwin, nseq), 512, 2 * spad_size(4096) * sizeof(uint64_t), st>>>(keys, perm0,
+                                                                                                perm1, g);
+  else
+    k_chunk_sort<1024><<<dim3(1, g.nwin, nseq), 1024, 2 * spad_size(8192) * sizeof(uint64_t), st>>>(keys, perm0,
+                                                                                                  perm1, g);
   return cudaGetLastError();
 }
 
