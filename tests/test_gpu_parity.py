@@ -110,6 +110,26 @@ def test_windowed_sort(dev, window):
     _attn_and_check(q, k, v, 128, sel, g, dev)
 
 
+@pytest.mark.parametrize("L,window", [(4097, 0), (8192, 0), (8193, 0), (16512, 8192), (25600, 12800)])
+def test_sort_path_boundaries(dev, L, window):
+    """Sorted sequences and windows on both sides of the one-CTA chunk sort's
+    limits (4096 keys on 512 threads, 8192 on 1024) and the clustered radix
+    sort beyond them: pi, the lists and the attention against the oracle."""
+    q, k, v = workloads.random_inputs(1, 2, L, 128, seed=L + window, scale=1.5)
+    sel, g = _select_and_check(q, k, 128, 4, 1.0, 3, window, dev)
+    _attn_and_check(q, k, v, 128, sel, g, dev)
+
+
+@pytest.mark.parametrize("B,kappa", [(128, 48), (64, 90)])
+def test_in_kernel_gathers_many_heads(dev, B, kappa):
+    """More heads than the gather look-ahead (ten heads at 32 tile pairs per
+    head) and enough key blocks per CTA for the attention kernel to copy the
+    later heads' rows itself: every query block against the oracle."""
+    q, k, v = workloads.random_inputs(1, 12, 8192, 128, seed=B + kappa, scale=1.5)
+    sel, g = _select_and_check(q, k, B, kappa, 1.0, 3, 0, dev)
+    _attn_and_check(q, k, v, B, sel, g, dev)
+
+
 def test_custom_scale(dev):
     q, k, v = workloads.random_inputs(1, 2, 1024, 128, seed=5)
     sel, g = _select_and_check(q, k, 128, 3, 1.0, 3, 0, dev)
