@@ -704,7 +704,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // kappa_first and [n_first, N) with budget kappa - kappa_first (isolated
 // prefill / generation selection); n_first == N is the plain top-kappa.
 // kRange = false: the part is the whole row; elements past N hold key 0,
-// which no candidate (>= 1) counts, so no range test is needed.
+// which no candidate (>= 1) counts, so no range test is needed.  The MSB-first
+// search stops once exactly k keys lie at or above the threshold so far.
 template <int KPL, bool kRange>
 __device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int lane, int lo, int hi,
                                                int k, uint32_t &T, int &need) {
@@ -719,6 +720,9 @@ __device__ __forceinline__ void part_threshold(const uint32_t (&keys)[KPL], int 
     }
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (cnt >= static_cast<uint32_t>(k)) T = cand;
+    // exactly k keys at or above T: they are the top k whatever T's lower
+    // bits, and the keys equal to T (need below) are all of them taken
+    if (cnt == static_cast<uint32_t>(k)) break;
   }
   uint32_t gt = 0;
 #pragma unroll
