@@ -120,16 +120,13 @@ def select_bytes(w, sort_q=True, sort_k=True, kappa=None):
 
 def launches_per_step(w):
     """Kernels the library launches per step (select + sparse attention) for
-    sort mode QK: a norm pass, a chunk sort and ceil(log2(L / 4096)) merge
-    passes (Q and K together in each), one statistics, one score and one
+    sort mode QK and no sort window: a norm pass (Q and K together), the sort
+    of Q and K together (one chunk-sort launch for sequences of up to 8192
+    tokens, else four radix passes), one statistics, one score and one
     top-kappa kernel; then the tile-pair list kernel, one row-gather kernel
     (Q, K, V) and the attention kernel."""
-    passes = 0
-    width = 4096
-    while width < w.seqlen:
-        width *= 2
-        passes += 1
-    select = 2 + passes + 3
+    sort = 1 if w.seqlen <= 8192 else 4
+    select = 1 + sort + 3
     attn = 3
     return select + attn
 
