@@ -764,20 +764,31 @@ struct GatherJobs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(256) k_gather_rows(const GatherJobs jobs, int64_t rows, int L) {
+__global__ void __launch_bounds__(256, 8) k_gather_rows(const GatherJobs jobs, int64_t rows, int L) {
   constexpr int VPR = D / 8;
   constexpr int RPW = 256 / VPR;
+  // the job's pointers by selection (an indexed parameter array would be
+  // copied to local memory)
   const int job = blockIdx.y;
-  const __nv_bfloat16 *in = jobs.in[job];
-  __nv_bfloat16 *out = jobs.out[job];
-  const int32_t *perm = jobs.perm[job];
+  const __nv_bfloat16 *in = job == 0 ? jobs.in[0] : (job == 1 ? jobs.in[1] : jobs.in[2]);
+  __nv_bfloat16 *out = job == 0 ? jobs.out[0] : (job == 1 ? jobs.out[1] : jobs.out[2]);
+  const int32_t *perm = job == 0 ? jobs.perm[0] : (job == 1 ? jobs.perm[1] : jobs.perm[2]);
   const int c = threadIdx.x % VPR;
   const int64_t row0 = static_cast<int64_t>(blockIdx.x) * RPW * kGatherRows + threadIdx.x / VPR;
+  // first row of the head of each row, carried from row to row (rows of a
+  // thread are RPW apart): one division per thread
+  int64_t hb = row0 - row0 % L;
+  int tk = static_cast<int>(row0 - hb);
   int64_t src[kGatherRows];
 #pragma unroll
   for (int u = 0; u < kGatherRows; ++u) {
     const int64_t row = row0 + u * RPW;
-    src[u] = (row < rows) ? (row / L) * L + min(max(__ldg(perm + row), 0), L - 1) : -1;
+    src[u] = (row < rows) ? hb + min(max(__ldg(perm + row), 0), L - 1) : -1;
+    tk += RPW;
+    while (tk >= L) {
+      tk -= L;
+      hb += L;
+    }
   }
   uint4 v[kGatherRows];
 #pragma unroll
